@@ -1,0 +1,419 @@
+"""Benchmark of the GB300 GEMM library: TFLOPS = 2MNK/t and roofline fraction.
+
+Default workload: FP32 SIMT GEMM, M = N = K = 8192, A, B, C row-major, values
+U[-1, 1) from seed 3 (the SIMT headline case).  The same run also measures the
+tensor-core headline case (FFN-shaped M=8192, N=14336, K=4096, N(0, 0.02) from
+seed 4, BF16 and TF32 inputs, FP32 C) and reports it under "modes".
+
+One step = one gemm_run of the whole workload through the C ABI with inputs
+resident in HBM.  Inputs are larger than L2, so no flush is needed.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the FP64 CPU oracle (the only reference this project
+has) on a bounded sample of the same workload on the host cores.  Under
+torchrun (N > 1) each rank runs an independent replica on its own GPU
+("scaling": "weak"); the time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOPS (2MNK/t) and % of GB300 FP32-SIMT / tensor-core roofline"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "fp32_8192_row"
+TC_WORKLOADS = ["ffn_bf16_8192x14336x4096", "ffn_tf32_8192x14336x4096"]
+
+# Fallback peaks (one earlier GB300 measurement) if MEASURED_PEAKS.json is absent.
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0}
+# Nominal dense tensor rates (PFLOP/s) used only to scale the measured BF16 peak
+# to TF32: a contraction is compared with the peak of its own input type.
+NOMINAL_PF = {"bf16": 2.25, "tf32": 1.1}
+
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# ncu capture of the kernel as it is now; None until captured for this version.
+# Key: workload name -> (bytes per launch, summary file under profiles/).
+NCU_TRAFFIC: dict[str, tuple[float, str]] = {}
+
+DESCRIPTIONS = {
+    "fp32_8192_row": "FP32 SIMT GEMM M=N=K=8192, A/B/C row-major, U[-1,1) seed 3",
+    "ffn_bf16_8192x14336x4096": "tensor-core GEMM, BF16 A/B, FP32 C, M=8192 N=14336 K=4096, N(0,0.02) seed 4",
+    "ffn_tf32_8192x14336x4096": "tensor-core GEMM, TF32 (FP32 storage), FP32 C, M=8192 N=14336 K=4096, N(0,0.02) seed 4",
+    "fp32_1024_colB": "FP32 SIMT GEMM M=N=K=1024, B column-major, U[-1,1) seed 1",
+    "fp32_4095x3073x2047_row": "FP32 SIMT GEMM M=4095 N=3073 K=2047, row-major, N(0,1) seed 2",
+    "fp32_128_row": "FP32 SIMT GEMM M=N=K=128, row-major, U[-1,1) seed 0",
+    "fp32_4096_row": "FP32 SIMT GEMM M=N=K=4096, row-major, U[-1,1) seed 3 (profiling size)",
+    "ffn_bf16_4096x7168x4096": "tensor-core GEMM, BF16, M=4096 N=7168 K=4096 (profiling size)",
+    "ffn_tf32_4096x7168x4096": "tensor-core GEMM, TF32, M=4096 N=7168 K=4096 (profiling size)",
+}
+
+
+# ---------------------------------------------------------------- host logic
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK}, "measured"
+    except (OSError, ValueError, KeyError):
+        return dict(FALLBACK), "fallback"
+
+
+def tensor_peak(dtype: str, peaks: dict, sustained: bool = False) -> float:
+    bf16 = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    return bf16 * NOMINAL_PF[dtype] / NOMINAL_PF["bf16"]
+
+
+def roofline_entry(bound, achieved, peak, unit, traffic, note):
+    return {"bound": bound, "achieved": round(achieved, 3), "peak": round(peak, 3),
+            "unit": unit, "frac": round(achieved / peak, 4) if peak else None,
+            "traffic": traffic, "peak_source": note}
+
+
+def aggregate(ms_per_rank, flops_per_rank_step):
+    """Whole-job throughput over ranks: total work / slowest rank's time."""
+    ms = max(ms_per_rank)
+    total = flops_per_rank_step * len(ms_per_rank)
+    return ms, total / (ms * 1e-3) / 1e12
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock, power and throttle reasons, kept only
+    for the wall-clock window [t0, t1] of the timed region."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.gpu), "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+            return
+        deadline = time.time() + 10
+        while time.time() < deadline and os.path.getsize(self.path) == 0:
+            time.sleep(0.05)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts + frac, float(parts[2]), float(parts[3]), parts[4], parts[5:]))
+            except (ValueError, IndexError):
+                continue
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05] or rows[-3:]
+        if not inside:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[4][1:5]) if v.strip() == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside),
+                "samples": len(inside), "reasons": reasons}
+
+
+# ---------------------------------------------------------------- GPU timing
+
+def time_device(run, stream, steps, warmup, counter=None):
+    """Run `warmup` untimed steps, then `steps` timed steps with a CUDA event
+    pair around each launch on `stream`.  Returns (total ms, per-step ms,
+    kernels launched in the timed region according to `counter`)."""
+    import torch
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    c0 = counter() if counter else 0
+    for i in range(steps):
+        starts[i].record(stream)
+        run()
+        ends[i].record(stream)
+    c1 = counter() if counter else 0
+    torch.cuda.synchronize()
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return starts[0].elapsed_time(ends[-1]), per, c1 - c0
+
+
+def bench_workload(g, name, steps, warmup, dist_ctx, peaks, peak_note, with_e2e, sampler=None):
+    import torch
+    from dense_gemm_sm100_gb300 import inputs as inp
+    from dense_gemm_sm100_gb300 import roofline as rl
+
+    w = inp.ALL_WORKLOADS[name]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    A, B = inp.make_workload(w)
+    A_d, B_d = A.to(dev), B.to(dev)
+    C_d = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def run():
+        g.run(A_d, B_d, C_d, w.layout_b, w.dtype, stream)
+
+    barrier(dist_ctx)
+    t0 = time.time()
+    total_ms, per, launches = time_device(run, stream, steps, warmup, lambda: g.launch_count)
+    t1 = time.time()
+    g.sync_status(stream)
+    barrier(dist_ctx)
+    ms_step = total_ms / steps
+    ms_all = all_gather_max(dist_ctx, ms_step)
+    ms_max, value = aggregate(ms_all, w.flops)
+    kernel_ms = statistics.mean(per)
+    achieved = w.flops / (kernel_ms * 1e-3) / 1e12
+    es = 2 if w.dtype == "bf16" else 4
+    if w.dtype == "f32":
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        peak = rl.fp32_simt_peak_tflops(sms, peaks["sm_max_mhz"])
+        roof = roofline_entry("alu", achieved, peak, UNIT, NCU_TRAFFIC.get(name, (None,))[0],
+                              f"derived: {sms} SMs x 128 FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz")
+    else:
+        peak = tensor_peak(w.dtype, peaks)
+        note = f"{peak_note} cuBLAS BF16 burst" + ("" if w.dtype == "bf16" else " x 1.1/2.25 (nominal TF32/BF16)")
+        roof = roofline_entry("tensor", achieved, peak, UNIT, NCU_TRAFFIC.get(name, (None,))[0], note)
+    res = {
+        "workload": name, "description": DESCRIPTIONS.get(name, name),
+        "M": w.M, "N": w.N, "K": w.K, "layout_b": "row" if w.layout_b == 0 else "col",
+        "dtype": w.dtype, "value": value, "ms_per_step": ms_max, "kernel_ms": kernel_ms,
+        "kernel_ms_min": min(per), "path": g.last_path, "roofline": roof,
+        "launches_timed": launches, "wall_window": (t0, t1),
+        "compulsory_bytes": rl.compulsory_bytes(w.M, w.N, w.K, es),
+    }
+    if with_e2e:
+        Ah = A.pin_memory()
+        Bh = B.pin_memory()
+        Ch = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
+
+        def run_host():
+            g.run_host(Ah, Bh, Ch, w.layout_b, w.dtype, stream)
+
+        e2e_steps = max(2, min(steps, 10))
+        e2e_ms, _, _ = time_device(run_host, stream, e2e_steps, 2)
+        g.sync_status(stream)
+        e2e_ms_all = all_gather_max(dist_ctx, e2e_ms / e2e_steps)
+        _, e2e_value = aggregate(e2e_ms_all, w.flops)
+        res["e2e"] = {"value": e2e_value, "unit": UNIT,
+                      "h2d_bytes_per_step": A.numel() * A.element_size() + B.numel() * B.element_size(),
+                      "d2h_bytes_per_step": w.M * w.N * 4,
+                      "ms_per_step": max(e2e_ms_all)}
+    del A_d, B_d, C_d
+    torch.cuda.empty_cache()
+    return res
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_sample(name, target_s):
+    """Time the FP64 oracle on a row sample of the workload sized to take
+    about target_s seconds; returns (TFLOP/s, seconds, rows, threads)."""
+    import oracle
+    from dense_gemm_sm100_gb300 import inputs as inp
+    w = inp.ALL_WORKLOADS[name]
+    A, B = inp.make_workload(w)
+    A64 = A.double().numpy()
+    B64 = B.double().numpy()
+    threads = oracle.default_threads()
+    rows = max(1, min(w.M, threads))
+    t = time.perf_counter()
+    oracle.gemm(A64[:rows], B64, w.layout_b)
+    dt = time.perf_counter() - t
+    rows = int(max(1, min(w.M, rows * target_s / max(dt, 1e-3))))
+    return A64, B64, w, rows, threads
+
+
+def time_oracle(A64, B64, w, rows):
+    import oracle
+    t = time.perf_counter()
+    oracle.gemm(A64[:rows], B64, w.layout_b)
+    dt = time.perf_counter() - t
+    return 2.0 * rows * w.N * w.K / dt / 1e12, dt
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return None
+    import torch
+    import torch.distributed as dist
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend)
+    return {"rank": dist.get_rank(), "world": dist.get_world_size(), "local": local}
+
+
+def barrier(ctx):
+    if ctx is not None:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def all_gather_max(ctx, value: float):
+    """Every rank's value (list), for max-over-ranks timing."""
+    if ctx is None:
+        return [value]
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    out = [torch.zeros_like(t) for _ in range(ctx["world"])]
+    dist.all_gather(out, t)
+    return [float(x.item()) for x in out]
+
+
+# ---------------------------------------------------------------- entry
+
+def run_reference(args, ctx):
+    """The reference arm: the FP64 CPU oracle, each step one row sample."""
+    if ctx is not None and ctx["rank"] != 0:
+        return 0
+    name = args.workload
+    A64, B64, w, rows, threads = oracle_sample(name, target_s=args.ref_step_s)
+    for _ in range(args.warmup):
+        time_oracle(A64, B64, w, max(1, rows // 8))
+    times = []
+    for _ in range(args.steps):
+        _, dt = time_oracle(A64, B64, w, rows)
+        times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    value = 2.0 * rows * w.N * w.K / (ms * 1e-3) / 1e12
+    sample = f"rows 0..{rows - 1} of A times all of B ({rows}x{w.N}x{w.K} of the {w.M}x{w.N}x{w.K} product)"
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS.get(name, name), "M": w.M, "N": w.N, "K": w.K},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-modes", action="store_true", help="skip the tensor-core workloads")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-s", type=float, default=2.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    ctx = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, ctx)
+
+    import torch
+    from dense_gemm_sm100_gb300 import gemm
+    dev_index = ctx["local"] if ctx else 0
+    torch.cuda.set_device(dev_index)
+    peaks, peak_note = load_peaks()
+    g = gemm.Gemm(dev_index)
+    rank0 = ctx is None or ctx["rank"] == 0
+
+    sampler = ClockSampler(dev_index) if rank0 else None
+    clocks = None
+    if sampler:
+        sampler.start()
+    main_res = bench_workload(g, args.workload, args.steps, args.warmup, ctx, peaks, peak_note,
+                              with_e2e=False)
+    if sampler:
+        sampler.stop()
+        clocks = sampler.summary(*main_res["wall_window"])
+    modes = []
+    if not args.no_modes:
+        for name in TC_WORKLOADS:
+            r = bench_workload(g, name, max(args.steps, 100), args.warmup, ctx, peaks, peak_note,
+                               with_e2e=False)
+            modes.append({k: r[k] for k in ("workload", "description", "dtype", "value",
+                                            "ms_per_step", "kernel_ms", "path", "roofline")})
+    e2e = None
+    if not args.no_e2e:
+        r = bench_workload(g, args.workload, min(args.steps, 10), args.warmup, ctx, peaks,
+                           peak_note, with_e2e=True)
+        e2e = r["e2e"]
+    cpu = None
+    if rank0 and ctx is None and not args.no_cpu_baseline:
+        A64, B64, w, rows, threads = oracle_sample(args.workload, target_s=args.cpu_seconds)
+        value, dt = time_oracle(A64, B64, w, rows)
+        cpu = {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"rows 0..{rows - 1} of A times all of B ({rows}x{w.N}x{w.K} of the "
+                         f"{w.M}x{w.N}x{w.K} product), {dt:.1f} s, FP64 with |a*b| sums"}
+    g.close()
+    if not rank0:
+        return 0
+    n = ctx["world"] if ctx else 1
+    line = {
+        "metric": METRIC, "value": main_res["value"], "unit": UNIT, "n_gpus": n,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": main_res["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": main_res["dtype"], "data": "synthetic",
+        "config": {"workload": main_res["description"], "M": main_res["M"], "N": main_res["N"],
+                   "K": main_res["K"], "layout_b": main_res["layout_b"], "path": main_res["path"],
+                   "l2": "inputs larger than L2 (A, B, C 768 MiB vs 129 MB L2); no flush",
+                   "parallelism": f"replicas{n}" if n > 1 else "single-gpu"},
+        "roofline": main_res["roofline"],
+        "kernel_ms": main_res["kernel_ms"],
+        "gpu_launches": main_res["launches_timed"],
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "modes": modes,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

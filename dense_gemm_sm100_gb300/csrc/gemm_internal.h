@@ -1,0 +1,65 @@
+// Host-side interface between the C ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace dg {
+
+// Geometry of the FP32 SIMT kernel (sgemm_simt.cu).  A tile of C is
+// kSimtBM x kSimtBN; K advances kSimtBK elements (128 bytes) per stage.
+constexpr int kSimtBM = 128;
+constexpr int kSimtBN = 128;
+constexpr int kSimtBK = 32;
+// TMA boxes, innermost dimension first.
+constexpr int kSimtBoxA[2] = {kSimtBK, kSimtBM};        // A rows, K contiguous
+constexpr int kSimtBoxBRow[2] = {32, kSimtBK};          // row-major B: 32 columns x BK rows
+constexpr int kSimtBoxBCol[2] = {kSimtBK, kSimtBN};     // column-major B: BN columns, K contiguous
+
+// Geometry of the tensor-core kernel (gemm_tc.cu).  A tile of C is
+// kTcBM x kTcBN; every stage holds 128 bytes of K per operand row, i.e.
+// 64 BF16 or 32 TF32 elements.
+constexpr int kTcBM = 128;
+constexpr int kTcBN = 256;
+constexpr int tc_bk(int elem_bytes) { return 128 / elem_bytes; }
+
+struct LaunchCommon {
+    int *status;          // device status word (0 = fine)
+    uint64_t timeout_ns;  // limit of every in-kernel wait
+    int grid;             // persistent CTAs to launch
+    int group_m;          // tile-order group height (tiles)
+    cudaStream_t stream;
+};
+
+// Each kernel family raises its dynamic shared-memory limit on the current
+// device.  Returns the first CUDA error.
+cudaError_t prepare_simt();
+cudaError_t prepare_tc();
+
+// FP32 SIMT GEMM.  tmA maps A (dims {K, M}), tmB maps the stored B
+// (row-major: dims {N, K}; column-major: dims {K, N}), both FP32 with a
+// 128-byte swizzle and the boxes above.
+cudaError_t launch_simt_f32(const CUtensorMap &tmA, const CUtensorMap &tmB, int layout_b,
+                            int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
+                            const LaunchCommon &lc);
+
+// Tensor-core GEMM; dtype is GEMM_TF32 or GEMM_BF16.  tmA/tmB as above with
+// 128-byte rows (BK elements) and the tensor-core boxes.
+cudaError_t launch_tc(int dtype, int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                      int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
+                      const LaunchCommon &lc);
+
+// dst[r*ldd + c] = src[r*lds + c] for r < rows, c < cols (elem_bytes 2 or 4).
+cudaError_t launch_repack(const void *src, int64_t lds, void *dst, int64_t ldd, int64_t rows,
+                          int64_t cols, int elem_bytes, int sm_count, cudaStream_t stream);
+
+// C[i*ldc + j] = 0 for i < M, j < N.
+cudaError_t launch_zero_fill(float *C, int64_t ldc, int64_t M, int64_t N, int sm_count,
+                             cudaStream_t stream);
+
+// Persistent-grid size a kernel wants for `tiles` output tiles.
+int simt_grid(int tiles, int sm_count);
+int tc_grid(int tiles, int sm_count);
+
+}  // namespace dg

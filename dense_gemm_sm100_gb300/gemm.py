@@ -1,0 +1,269 @@
+"""Python binding of the C ABI in include/gemm.h (argument marshalling only).
+
+The functions ``gemm_create``, ``gemm_run``, ``gemm_run_host``,
+``gemm_destroy``, ``gemm_validate``, ``gemm_sync_status``,
+``gemm_set_option``, ``gemm_last_error_string``, ``gemm_status_string``,
+``gemm_last_path``, ``gemm_launch_count`` and ``gemm_version`` take and return
+the same plain values as their C counterparts (pointers as ints).  ``Gemm``
+wraps a handle for torch tensors.  Every GEMM step runs in the library's CUDA
+kernels; there is no other code path, and calling anything here without the
+built library raises ``GemmLibraryMissing``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+GEMM_B_ROW_MAJOR = 0
+GEMM_B_COL_MAJOR = 1
+GEMM_F32 = 0
+GEMM_TF32 = 1
+GEMM_BF16 = 2
+
+GEMM_OK = 0
+GEMM_ERR_INVALID = -1
+GEMM_ERR_ALIGNMENT = -2
+GEMM_ERR_CUDA = -3
+GEMM_ERR_TIMEOUT = -4
+GEMM_ERR_DEVICE = -5
+GEMM_ERR_NOMEM = -6
+
+GEMM_OPT_FORCE_REPACK = 1
+GEMM_OPT_WAIT_TIMEOUT_NS = 2
+GEMM_OPT_SIMT_GROUP_M = 3
+GEMM_OPT_TC_GROUP_M = 4
+GEMM_OPT_MAX_CTAS = 5
+
+DTYPES = {"f32": GEMM_F32, "tf32": GEMM_TF32, "bf16": GEMM_BF16}
+LAYOUTS = {"row": GEMM_B_ROW_MAJOR, "col": GEMM_B_COL_MAJOR}
+
+LIB_PATH = _build.LIB_PATH
+
+
+class GemmLibraryMissing(RuntimeError):
+    """The CUDA library has not been built (run ``__graft_entry__.build()``)."""
+
+
+class GemmError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{gemm_status_string(code)}: {message}")
+        self.code = code
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library():
+    """Load ``libdense_gemm_gb300.so`` (raises GemmLibraryMissing if absent)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise GemmLibraryMissing(
+                f"{LIB_PATH} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(LIB_PATH)
+        i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+        run_args = [vp, ci, i64, i64, i64, vp, i64, vp, i64, vp, i64, ci, vp]
+        sig = {
+            "gemm_create": ([ctypes.POINTER(vp), ci], ci),
+            "gemm_destroy": ([vp], ci),
+            "gemm_run": (run_args, ci),
+            "gemm_run_host": (run_args, ci),
+            "gemm_validate": ([ci, i64, i64, i64, vp, i64, vp, i64, vp, i64, ci], ci),
+            "gemm_sync_status": ([vp, vp], ci),
+            "gemm_set_option": ([vp, ci, i64], ci),
+            "gemm_last_error_string": ([vp], ctypes.c_char_p),
+            "gemm_status_string": ([ci], ctypes.c_char_p),
+            "gemm_last_path": ([vp], ctypes.c_char_p),
+            "gemm_launch_count": ([vp], i64),
+            "gemm_version": ([], ci),
+        }
+        for name, (argtypes, restype) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = argtypes
+            fn.restype = restype
+        _lib = lib
+        return lib
+
+
+# ----------------------------------------------------------- C-named functions
+
+def gemm_version() -> int:
+    return load_library().gemm_version()
+
+
+def gemm_status_string(code: int) -> str:
+    return load_library().gemm_status_string(code).decode()
+
+
+def gemm_create(device: int = 0) -> int:
+    h = ctypes.c_void_p()
+    rc = load_library().gemm_create(ctypes.byref(h), device)
+    if rc != GEMM_OK:
+        raise GemmError(rc, f"gemm_create(device={device}) failed")
+    return h.value
+
+
+def gemm_destroy(handle: int) -> int:
+    return load_library().gemm_destroy(handle)
+
+
+def gemm_run(handle, layout_b, M, N, K, A, lda, B, ldb, C, ldc, dtype, stream) -> int:
+    return load_library().gemm_run(handle, layout_b, M, N, K, A, lda, B, ldb, C, ldc, dtype, stream)
+
+
+def gemm_run_host(handle, layout_b, M, N, K, A, lda, B, ldb, C, ldc, dtype, stream) -> int:
+    return load_library().gemm_run_host(handle, layout_b, M, N, K, A, lda, B, ldb, C, ldc,
+                                        dtype, stream)
+
+
+def gemm_validate(layout_b, M, N, K, A, lda, B, ldb, C, ldc, dtype) -> int:
+    return load_library().gemm_validate(layout_b, M, N, K, A, lda, B, ldb, C, ldc, dtype)
+
+
+def gemm_sync_status(handle, stream) -> int:
+    return load_library().gemm_sync_status(handle, stream)
+
+
+def gemm_set_option(handle, option, value) -> int:
+    return load_library().gemm_set_option(handle, option, value)
+
+
+def gemm_last_error_string(handle) -> str:
+    return load_library().gemm_last_error_string(handle).decode()
+
+
+def gemm_last_path(handle) -> str:
+    return load_library().gemm_last_path(handle).decode()
+
+
+def gemm_launch_count(handle) -> int:
+    return load_library().gemm_launch_count(handle)
+
+
+# ------------------------------------------------------------- torch wrapper
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+class Gemm:
+    """A library handle used with torch tensors.
+
+    ``run(A, B, C, layout_b, dtype)`` computes C = A·B on the GPU: A is (M, K)
+    row-major, B is (K, N) for ``layout_b="row"`` or (N, K) for ``"col"``
+    (each row holding one column of the logical B), C is (M, N).  Rows may be
+    padded (any stride(0) >= columns, stride(1) == 1).  The call is queued on
+    ``stream`` (default: torch's current stream) and returns at once.
+    """
+
+    def __init__(self, device: int = 0):
+        self.device = device
+        self.handle = gemm_create(device)
+
+    def close(self):
+        if self.handle:
+            gemm_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _check(self, rc: int):
+        if rc != GEMM_OK:
+            raise GemmError(rc, gemm_last_error_string(self.handle))
+
+    def set_option(self, option: int, value: int):
+        self._check(gemm_set_option(self.handle, option, int(value)))
+
+    @staticmethod
+    def _dims(A, B, layout_b):
+        M, K = A.shape
+        if layout_b == GEMM_B_ROW_MAJOR:
+            Kb, N = B.shape
+        else:
+            N, Kb = B.shape
+        if Kb != K:
+            raise ValueError(f"inner dimensions differ: A has K={K}, B has K={Kb}")
+        return M, N, K
+
+    @staticmethod
+    def _ld(t):
+        if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+            raise ValueError("operands must be 2-D with unit stride along rows")
+        return max(t.stride(0), t.shape[1], 1)
+
+    def run(self, A, B, C, layout_b="row", dtype="f32", stream=None):
+        lb = LAYOUTS.get(layout_b, layout_b)
+        dt = DTYPES.get(dtype, dtype)
+        M, N, K = self._dims(A, B, lb)
+        if tuple(C.shape) != (M, N):
+            raise ValueError(f"C has shape {tuple(C.shape)}, expected {(M, N)}")
+        self._check(gemm_run(self.handle, lb, M, N, K, A.data_ptr(), self._ld(A), B.data_ptr(),
+                             self._ld(B), C.data_ptr(), self._ld(C), dt, _stream_handle(stream)))
+        return C
+
+    def run_host(self, A, B, C, layout_b="row", dtype="f32", stream=None):
+        """As ``run`` with CPU tensors (pinned for asynchronous copies): the
+        library copies A and B in, runs, and copies C out on ``stream``."""
+        lb = LAYOUTS.get(layout_b, layout_b)
+        dt = DTYPES.get(dtype, dtype)
+        M, N, K = self._dims(A, B, lb)
+        self._check(gemm_run_host(self.handle, lb, M, N, K, A.data_ptr(), self._ld(A),
+                                  B.data_ptr(), self._ld(B), C.data_ptr(), self._ld(C), dt,
+                                  _stream_handle(stream)))
+        return C
+
+    def sync_status(self, stream=None):
+        """Wait for ``stream`` and raise GemmError if an in-kernel wait expired."""
+        self._check(gemm_sync_status(self.handle, _stream_handle(stream)))
+
+    @property
+    def last_path(self) -> str:
+        return gemm_last_path(self.handle)
+
+    @property
+    def launch_count(self) -> int:
+        return gemm_launch_count(self.handle)
+
+
+def matmul(A, B, layout_b="row", dtype="f32", out=None, stream=None, handle: Gemm | None = None):
+    """Allocate C (float32, on A's device) if needed and return C = A·B."""
+    import torch
+    lb = LAYOUTS.get(layout_b, layout_b)
+    M, N, _ = Gemm._dims(A, B, lb)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    g = handle or _default_handle(A.device.index or 0)
+    return g.run(A, B, out, lb, dtype, stream)
+
+
+_handles: dict[int, Gemm] = {}
+
+
+def _default_handle(device: int) -> Gemm:
+    with _lock:
+        h = _handles.get(device)
+    if h is None:
+        h = Gemm(device)
+        with _lock:
+            _handles[device] = h
+    return h

@@ -65,6 +65,18 @@ WORKLOADS = {
 }
 
 
+# Smaller cases of the same kernels, sized for profiler captures: operands
+# still larger than L2 (129 MB) but a few hundred MB in total.
+PROFILE_WORKLOADS = {
+    "fp32_4096_row": Workload("fp32_4096_row", 4096, 4096, 4096, B_ROW_MAJOR, "uniform", 3),
+    "ffn_bf16_4096x7168x4096": Workload("ffn_bf16_4096x7168x4096", 4096, 7168, 4096,
+                                        B_ROW_MAJOR, "normal", 4, 0.02, BF16),
+    "ffn_tf32_4096x7168x4096": Workload("ffn_tf32_4096x7168x4096", 4096, 7168, 4096,
+                                        B_ROW_MAJOR, "normal", 4, 0.02, TF32),
+}
+ALL_WORKLOADS = {**WORKLOADS, **PROFILE_WORKLOADS}
+
+
 def _draw(gen: torch.Generator, shape, dist: str, sigma: float) -> torch.Tensor:
     if dist == "uniform":
         return torch.rand(shape, generator=gen, dtype=torch.float32) * 2.0 - 1.0

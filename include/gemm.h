@@ -1,0 +1,163 @@
+/*
+ * dense_gemm_sm100_gb300 — single-GPU dense GEMM C = A·B for NVIDIA GB300
+ * (sm_103a), behind a plain C ABI.
+ *
+ * The operation (its definition and the layouts) comes from two pages:
+ *
+ *  - "GEMM 性能优化", section 指标与目标 and 台阶 1 (Shared Memory Tiling):
+ *    C = A·B accumulates along K; 2·M·N·K flops; TFLOPS = 2MNK / (t·1e12).
+ *  - "PMPP Chapter 06: Performance considerations", section 1 (Corner
+ *    Turning example): A and C row-major, B column-major with element (k, j)
+ *    at B[j*K + k]; out-of-range tile elements count as zero and only the
+ *    C elements inside M x N are written.
+ *
+ * Semantics of every run entry point:
+ *
+ *     C[i*ldc + j] = sum_{k < K} A[i*lda + k] * B(k, j)   for i < M, j < N
+ *     B(k, j) = B[k*ldb + j]   (GEMM_B_ROW_MAJOR)
+ *     B(k, j) = B[j*ldb + k]   (GEMM_B_COL_MAJOR, the corner-turning case)
+ *
+ * C is overwritten (no alpha/beta); C elements outside the M x N box (the
+ * ldc padding) are never touched.  Leading dimensions count elements.  K = 0
+ * writes C = 0 (the empty sum).  M = 0 or N = 0 does nothing and succeeds.
+ * C must not overlap A or B.  The order of the additions inside a sum is the
+ * library's choice but fixed: repeated calls give bit-identical results.
+ *
+ * Compute modes (the `dtype` argument):
+ *
+ *   GEMM_F32   A, B, C float.  FP32 fused multiply-adds on the CUDA cores
+ *              (SIMT), accumulation in FP32.
+ *   GEMM_TF32  A, B, C float.  Tensor cores (tcgen05.mma kind::tf32): the
+ *              operands enter the multiplier as TF32 (10-bit mantissa);
+ *              products accumulate in FP32.
+ *   GEMM_BF16  A, B bfloat16 (uint16 bit patterns), C float.  Tensor cores
+ *              (tcgen05.mma kind::f16 with BF16 inputs), FP32 accumulation.
+ *
+ * Ownership and threading: the caller owns A, B, C and the stream.  A handle
+ * owns a small device status word and a device workspace that grows on
+ * demand (used to re-pack operands whose address or leading dimension is not
+ * a multiple of 16 bytes, and by gemm_run_host).  Calls on one handle must be
+ * issued from one host thread at a time and be ordered on the GPU (one
+ * stream, or streams the caller orders), because they share the workspace.
+ *
+ * Errors: every function returns GEMM_OK (0) or a negative GEMM_ERR_* code.
+ * Argument errors are detected on the host before anything is launched.
+ * gemm_last_error_string() describes the last failure on a handle.
+ */
+#ifndef DENSE_GEMM_SM100_GB300_GEMM_H
+#define DENSE_GEMM_SM100_GB300_GEMM_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GEMM_VERSION 1
+
+/* Storage of B (the logical K x N operand). */
+#define GEMM_B_ROW_MAJOR 0 /* B[k*ldb + j], ldb >= N */
+#define GEMM_B_COL_MAJOR 1 /* B[j*ldb + k], ldb >= K (corner-turning case) */
+
+/* Compute modes, see above. */
+#define GEMM_F32 0
+#define GEMM_TF32 1
+#define GEMM_BF16 2
+
+/* Return codes. */
+#define GEMM_OK 0
+#define GEMM_ERR_INVALID (-1)   /* null pointer, negative size, ld too small, unknown enum */
+#define GEMM_ERR_ALIGNMENT (-2) /* a pointer not aligned to its element size */
+#define GEMM_ERR_CUDA (-3)      /* a CUDA call failed; see gemm_last_error_string */
+#define GEMM_ERR_TIMEOUT (-4)   /* a kernel's bounded wait expired (reported by gemm_sync_status) */
+#define GEMM_ERR_DEVICE (-5)    /* no usable device, or not a compute capability 10.3 GPU */
+#define GEMM_ERR_NOMEM (-6)     /* workspace or host bookkeeping allocation failed */
+
+/* Options for gemm_set_option. */
+#define GEMM_OPT_FORCE_REPACK 1   /* 1: always stage A and B through the workspace (tests) */
+#define GEMM_OPT_WAIT_TIMEOUT_NS 2 /* limit of every in-kernel wait, nanoseconds (default 4e9) */
+#define GEMM_OPT_SIMT_GROUP_M 3   /* tile-order group height in tiles for the FP32 kernel */
+#define GEMM_OPT_TC_GROUP_M 4     /* tile-order group height in tiles for the tensor-core kernel */
+#define GEMM_OPT_MAX_CTAS 5       /* cap on persistent CTAs (0 = one per SM) */
+
+typedef struct gemm_ctx *gemm_handle_t;
+
+/*
+ * Create a handle bound to CUDA device `device` (which becomes current on the
+ * calling thread).  Fails with GEMM_ERR_DEVICE when the device is missing or
+ * is not compute capability 10.3 (GB300).  *out is set only on success.
+ */
+int gemm_create(gemm_handle_t *out, int device);
+
+/* Release the handle and its device memory.  NULL is accepted. */
+int gemm_destroy(gemm_handle_t h);
+
+/*
+ * C = A·B on `stream` (device pointers; see the semantics above).
+ * Asynchronous: returns once the work is queued.  A, B and C must stay valid
+ * until the stream has executed it.  For GEMM_F32/GEMM_TF32, A, B and C are
+ * float*; for GEMM_BF16, A and B point to bfloat16 values.  A and B must be
+ * aligned to their element size, C to 4 bytes (else GEMM_ERR_ALIGNMENT).
+ * Operands whose pointer or leading dimension is not a multiple of 16 bytes
+ * are first re-packed into the handle's workspace by a device kernel (part of
+ * the queued work).  A wait that expires inside a kernel is reported by
+ * gemm_sync_status, not here.
+ */
+int gemm_run(gemm_handle_t h, int layout_b, int64_t M, int64_t N, int64_t K,
+             const void *A, int64_t lda, const void *B, int64_t ldb,
+             float *C, int64_t ldc, int dtype, cudaStream_t stream);
+
+/*
+ * As gemm_run, but A, B and C are HOST pointers.  The call copies A and B
+ * into the handle's workspace (one cudaMemcpy2DAsync each), runs the GEMM,
+ * copies C back (one cudaMemcpy2DAsync), all on `stream`, and returns without
+ * waiting: the host buffers must stay valid and C must not be read until the
+ * stream has been synchronised.  Pinned (page-locked) host memory makes the
+ * copies asynchronous; pageable memory works but the copies block.
+ */
+int gemm_run_host(gemm_handle_t h, int layout_b, int64_t M, int64_t N, int64_t K,
+                  const void *A_host, int64_t lda, const void *B_host, int64_t ldb,
+                  float *C_host, int64_t ldc, int dtype, cudaStream_t stream);
+
+/*
+ * Check the arguments of a run without touching the GPU: returns GEMM_OK,
+ * GEMM_ERR_INVALID or GEMM_ERR_ALIGNMENT exactly as gemm_run would.
+ */
+int gemm_validate(int layout_b, int64_t M, int64_t N, int64_t K,
+                  const void *A, int64_t lda, const void *B, int64_t ldb,
+                  const float *C, int64_t ldc, int dtype);
+
+/*
+ * Wait for `stream`, then read and clear the handle's device status word.
+ * Returns GEMM_OK, GEMM_ERR_TIMEOUT when an in-kernel wait expired since the
+ * last check (the kernel then left C incomplete and returned), or
+ * GEMM_ERR_CUDA when the stream reports an error.
+ */
+int gemm_sync_status(gemm_handle_t h, cudaStream_t stream);
+
+/* Set an option (GEMM_OPT_*).  Returns GEMM_ERR_INVALID for an unknown
+ * option or an out-of-range value. */
+int gemm_set_option(gemm_handle_t h, int option, int64_t value);
+
+/* Human-readable description of the last failure on `h` ("" if none). */
+const char *gemm_last_error_string(gemm_handle_t h);
+
+/* Name of a GEMM_OK / GEMM_ERR_* code. */
+const char *gemm_status_string(int code);
+
+/* Name of the kernel path the last successful run on `h` queued, e.g.
+ * "simt_f32_128x128_rowB" or "tc_bf16_128x256_rowB+repack". */
+const char *gemm_last_path(gemm_handle_t h);
+
+/* Number of kernels this handle has launched so far (all paths). */
+int64_t gemm_launch_count(gemm_handle_t h);
+
+/* GEMM_VERSION of the library. */
+int gemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DENSE_GEMM_SM100_GB300_GEMM_H */

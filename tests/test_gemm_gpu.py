@@ -1,0 +1,273 @@
+"""GPU parity of the C-ABI GEMM against the FP64 oracle, element by element.
+
+Every case draws seeded inputs (dense_gemm_sm100_gb300.inputs), runs the
+library through its C ABI on cuda:0, and checks |C_gpu - C_ref| <= tol * S
+per element (tests/_parity.py).  Integer-valued inputs make every mode exact,
+so those cases must match bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+from dense_gemm_sm100_gb300 import inputs as inp
+from tests._parity import TOL, assert_parity, to_f64
+
+pytestmark = pytest.mark.gpu
+
+MODES = ["f32", "tf32", "bf16"]
+ROW, COL = inp.B_ROW_MAJOR, inp.B_COL_MAJOR
+
+
+@pytest.fixture(scope="module")
+def g():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dense_gemm_sm100_gb300 import build, gemm
+    build.build()
+    h = gemm.Gemm(0)
+    yield h
+    h.close()
+
+
+def run_gpu(g, A, B, layout, mode, C=None):
+    dev = torch.device("cuda", 0)
+    A_d, B_d = A.to(dev), B.to(dev)
+    M = A.shape[0]
+    N = B.shape[1] if layout == ROW else B.shape[0]
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float32, device=dev)
+    g.run(A_d, B_d, C, layout, mode)
+    g.sync_status()
+    torch.cuda.synchronize()
+    return C
+
+
+def oracle_of(oracle_mod, A, B, layout):
+    return oracle_mod.gemm(to_f64(A), to_f64(B), layout)
+
+
+SMALL_SHAPES = [
+    (1, 1, 1), (3, 5, 7), (16, 16, 16), (128, 128, 128), (129, 257, 33),
+    (200, 300, 100), (255, 129, 127), (300, 520, 260), (64, 1000, 65), (1000, 40, 300),
+]
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("layout", [ROW, COL])
+@pytest.mark.parametrize("shape", SMALL_SHAPES)
+def test_small_shapes_random(g, oracle_mod, mode, layout, shape):
+    M, N, K = shape
+    A, B = inp.make_operands(M, N, K, layout_b=layout, dist="normal",
+                             seed=M * 7 + N * 3 + K, dtype=mode)
+    C = run_gpu(g, A, B, layout, mode)
+    Cr, S = oracle_of(oracle_mod, A, B, layout)
+    assert_parity(C, Cr, S, TOL[mode], f"{mode} layout={layout} {shape}")
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("layout", [ROW, COL])
+def test_integer_inputs_bit_exact(g, oracle_mod, mode, layout):
+    M, N, K = 257, 515, 300
+    A, B = inp.make_integer_operands(M, N, K, layout_b=layout, seed=5, dtype=mode)
+    C = run_gpu(g, A, B, layout, mode)
+    Cr, _ = oracle_of(oracle_mod, A, B, layout)
+    assert np.array_equal(to_f64(C), Cr)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_padding_and_neighbours_untouched(g, oracle_mod, mode):
+    """Only C[i, j] with i < M and j < N is written ("PMPP Chapter 06",
+    corner-turning example: guarded stores)."""
+    M, N, K = 131, 261, 77
+    A, B = inp.make_operands(M, N, K, seed=9, dtype=mode)
+    dev = torch.device("cuda", 0)
+    big = torch.full((M + 3, N + 13), float("nan"), dtype=torch.float32, device=dev)
+    C = big[1:M + 1, 4:N + 4]  # ldc = N + 13, guard rows and columns on each side
+    run_gpu(g, A, B, ROW, mode, C=C)
+    Cr, S = oracle_of(oracle_mod, A, B, ROW)
+    assert_parity(C, Cr, S, TOL[mode])
+    host = big.cpu()
+    mask = torch.ones_like(host, dtype=torch.bool)
+    mask[1:M + 1, 4:N + 4] = False
+    assert torch.isnan(host[mask]).all()
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("layout", [ROW, COL])
+def test_deterministic(g, mode, layout):
+    A, B = inp.make_operands(300, 600, 500, layout_b=layout, seed=3, dtype=mode)
+    C1 = run_gpu(g, A, B, layout, mode).cpu()
+    C2 = run_gpu(g, A, B, layout, mode).cpu()
+    assert torch.equal(C1, C2)
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("layout", [ROW, COL])
+def test_blocked_matrix_identity(g, oracle_mod, mode, layout):
+    """Sum of the products over two K slices equals the full product ("GEMM
+    性能优化", 台阶 1).  The slices start at pointer offsets, so the second one
+    is generally not 16-byte aligned and goes through the re-pack path.
+    Integer inputs: exact."""
+    M, N, K, k0 = 190, 330, 300, 137
+    A, B = inp.make_integer_operands(M, N, K, layout_b=layout, seed=17, dtype=mode)
+    dev = torch.device("cuda", 0)
+    A_d, B_d = A.to(dev), B.to(dev)
+    full = torch.empty((M, N), dtype=torch.float32, device=dev)
+    p1 = torch.empty_like(full)
+    p2 = torch.empty_like(full)
+    g.run(A_d, B_d, full, layout, mode)
+    if layout == ROW:
+        g.run(A_d[:, :k0], B_d[:k0, :], p1, layout, mode)
+        g.run(A_d[:, k0:], B_d[k0:, :], p2, layout, mode)
+    else:
+        g.run(A_d[:, :k0], B_d[:, :k0], p1, layout, mode)
+        g.run(A_d[:, k0:], B_d[:, k0:], p2, layout, mode)
+    g.sync_status()
+    assert torch.equal((p1 + p2).cpu(), full.cpu())
+    Cr, _ = oracle_of(oracle_mod, A, B, layout)
+    assert np.array_equal(to_f64(full), Cr)
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("layout", [ROW, COL])
+def test_unaligned_leading_dimensions(g, oracle_mod, mode, layout):
+    """Odd leading dimensions and an offset base pointer (re-pack path)."""
+    M, N, K = 97, 203, 151
+    A, B = inp.make_operands(M, N, K, layout_b=layout, seed=23, dist="normal", dtype=mode)
+    dev = torch.device("cuda", 0)
+    Ap = torch.zeros((M, K + 3), dtype=A.dtype, device=dev)
+    Ap[:, 1:K + 1] = A.to(dev)
+    rows_b, cols_b = B.shape
+    Bp = torch.zeros((rows_b, cols_b + 5), dtype=B.dtype, device=dev)
+    Bp[:, 1:cols_b + 1] = B.to(dev)
+    Cbig = torch.zeros((M, N + 1), dtype=torch.float32, device=dev)
+    C = Cbig[:, :N]
+    g.run(Ap[:, 1:K + 1], Bp[:, 1:cols_b + 1], C, layout, mode)
+    g.sync_status()
+    assert "repackA" in g.last_path and "repackB" in g.last_path
+    Cr, S = oracle_of(oracle_mod, A, B, layout)
+    assert_parity(C, Cr, S, TOL[mode])
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_forced_repack_gives_same_bits(g, mode):
+    from dense_gemm_sm100_gb300 import gemm
+    A, B = inp.make_operands(160, 288, 192, seed=31, dtype=mode)
+    C1 = run_gpu(g, A, B, ROW, mode).cpu()
+    g.set_option(gemm.GEMM_OPT_FORCE_REPACK, 1)
+    try:
+        C2 = run_gpu(g, A, B, ROW, mode).cpu()
+        assert "repack" in g.last_path
+    finally:
+        g.set_option(gemm.GEMM_OPT_FORCE_REPACK, 0)
+    assert torch.equal(C1, C2)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_layout_invariance(g, mode):
+    """The same logical B stored either way gives the same C."""
+    A, Br = inp.make_operands(200, 333, 271, layout_b=ROW, seed=41, dtype=mode)
+    _, Bc = inp.make_operands(200, 333, 271, layout_b=COL, seed=41, dtype=mode)
+    C1 = run_gpu(g, A, Br, ROW, mode).cpu()
+    C2 = run_gpu(g, A, Bc, COL, mode).cpu()
+    if mode == "f32":
+        assert torch.equal(C1, C2)  # same k order per element in both layouts
+    else:
+        assert torch.allclose(C1, C2, rtol=0, atol=1e-5 * float(C1.abs().max()) + 1e-30)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_k_zero_writes_zeros(g, mode):
+    dev = torch.device("cuda", 0)
+    dt = torch.bfloat16 if mode == "bf16" else torch.float32
+    A = torch.empty((5, 0), dtype=dt, device=dev)
+    B = torch.empty((0, 9), dtype=dt, device=dev)
+    C = torch.full((5, 9), 3.0, device=dev)
+    g.run(A, B, C, ROW, mode)
+    g.sync_status()
+    assert torch.equal(C.cpu(), torch.zeros(5, 9))
+
+
+def test_empty_output_is_noop(g):
+    dev = torch.device("cuda", 0)
+    A = torch.ones((0, 4), device=dev)
+    B = torch.ones((4, 6), device=dev)
+    C = torch.empty((0, 6), device=dev)
+    g.run(A, B, C)
+    g.sync_status()
+    assert g.last_path == "noop"
+
+
+def test_errors_are_reported(g):
+    from dense_gemm_sm100_gb300 import gemm
+    dev = torch.device("cuda", 0)
+    A = torch.ones((4, 4), device=dev)
+    rc = gemm.gemm_run(g.handle, 0, 4, 4, 4, A.data_ptr(), 3, A.data_ptr(), 4, A.data_ptr(), 4, 0, 0)
+    assert rc == gemm.GEMM_ERR_INVALID
+    assert "lda" in gemm.gemm_last_error_string(g.handle)
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("layout", [ROW, COL])
+def test_run_host_matches_device(g, mode, layout):
+    A, B = inp.make_operands(211, 390, 300, layout_b=layout, seed=51, dtype=mode)
+    Cd = run_gpu(g, A, B, layout, mode).cpu()
+    Ch = torch.empty((211, 390), dtype=torch.float32).pin_memory()
+    g.run_host(A.pin_memory(), B.pin_memory(), Ch, layout, mode)
+    g.sync_status()
+    assert g.last_path.startswith("host+")
+    assert torch.equal(Cd, Ch)
+
+
+def test_launch_count_increments(g):
+    before = g.launch_count
+    A, B = inp.make_operands(64, 64, 64, seed=1)
+    run_gpu(g, A, B, ROW, "f32")
+    assert g.launch_count == before + 1
+
+
+# ------------------------------------------------------- the five workloads
+
+def _sampled_check(g, oracle_mod, w, n_rows=40, n_cols=40):
+    A, B = inp.make_workload(w)
+    dev = torch.device("cuda", 0)
+    A_d, B_d = A.to(dev), B.to(dev)
+    C = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
+    g.run(A_d, B_d, C, w.layout_b, w.dtype)
+    g.sync_status()
+    rows = inp.sample_indices(w.M, n_rows, seed=w.seed + 100)
+    cols = inp.sample_indices(w.N, n_cols, seed=w.seed + 200)
+    Cs = C[torch.tensor(rows, device=dev)][:, torch.tensor(cols, device=dev)]
+    Cr, S = oracle_mod.gemm_sampled(to_f64(A), to_f64(B), rows, cols, w.layout_b)
+    return assert_parity(Cs, Cr, S, TOL[w.dtype], w.name)
+
+
+@pytest.mark.parametrize("name", ["fp32_128_row", "fp32_1024_colB"])
+def test_workload_full(g, oracle_mod, name):
+    w = inp.WORKLOADS[name]
+    A, B = inp.make_workload(w)
+    C = run_gpu(g, A, B, w.layout_b, w.dtype)
+    Cr, S = oracle_of(oracle_mod, A, B, w.layout_b)
+    assert_parity(C, Cr, S, TOL[w.dtype], name)
+
+
+def test_workload_ragged_4095x3073x2047(g, oracle_mod):
+    """Non-tile-multiple edges with tight (not 16-byte multiple) leading
+    dimensions: checked on every row in a band at each edge and a sample of
+    the interior."""
+    w = inp.WORKLOADS["fp32_4095x3073x2047_row"]
+    A, B = inp.make_workload(w)
+    C = run_gpu(g, A, B, w.layout_b, w.dtype)
+    assert "repackA" in g.last_path and "repackB" in g.last_path
+    rows = sorted(set(range(0, 130)) | set(range(w.M - 130, w.M)) |
+                  set(inp.sample_indices(w.M, 64, seed=7)))
+    cols = sorted(set(range(0, 260)) | set(range(w.N - 260, w.N)) |
+                  set(inp.sample_indices(w.N, 64, seed=8)))
+    Cr, S = oracle_mod.gemm_sampled(to_f64(A), to_f64(B), rows, cols, w.layout_b)
+    assert_parity(C[rows][:, cols], Cr, S, TOL[w.dtype], w.name)
+
+
+@pytest.mark.parametrize("name", ["fp32_8192_row", "ffn_bf16_8192x14336x4096",
+                                  "ffn_tf32_8192x14336x4096"])
+def test_workload_sampled(g, oracle_mod, name):
+    _sampled_check(g, oracle_mod, inp.WORKLOADS[name])
