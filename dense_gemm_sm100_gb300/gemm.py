@@ -3,7 +3,8 @@
 The functions ``gemm_create``, ``gemm_run``, ``gemm_run_host``,
 ``gemm_destroy``, ``gemm_validate``, ``gemm_sync_status``,
 ``gemm_set_option``, ``gemm_last_error_string``, ``gemm_status_string``,
-``gemm_last_path``, ``gemm_launch_count`` and ``gemm_version`` take and return
+``gemm_last_path``, ``gemm_launch_count``, ``gemm_version`` and
+``gemm_run_noalloc`` take and return
 the same plain values as their C counterparts (pointers as ints).  ``Gemm``
 wraps a handle for torch tensors.  Every GEMM step runs in the library's CUDA
 kernels; there is no other code path, and calling anything here without the
@@ -83,6 +84,7 @@ def load_library():
             "gemm_last_path": ([vp], ctypes.c_char_p),
             "gemm_launch_count": ([vp], i64),
             "gemm_version": ([], ci),
+            "gemm_run_noalloc": ([ci, i64, i64, i64, vp, i64, vp, i64, vp, i64, ci, vp], ci),
         }
         for name, (argtypes, restype) in sig.items():
             fn = getattr(lib, name)
@@ -145,6 +147,17 @@ def gemm_last_path(handle) -> str:
 
 def gemm_launch_count(handle) -> int:
     return load_library().gemm_launch_count(handle)
+
+
+def gemm_run_noalloc(layout_b, M, N, K, A, lda, B, ldb, C, ldc, dtype, stream) -> int:
+    """C = A·B with no device allocation (no handle; the current device's
+    static scratch holds re-packed operands, at most
+    GEMM_NOALLOC_SCRATCH_BYTES).  For callers that cannot allocate."""
+    return load_library().gemm_run_noalloc(layout_b, M, N, K, A, lda, B, ldb, C, ldc, dtype,
+                                           stream)
+
+
+GEMM_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
 # ------------------------------------------------------------- torch wrapper

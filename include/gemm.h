@@ -156,6 +156,41 @@ int64_t gemm_launch_count(gemm_handle_t h);
 /* GEMM_VERSION of the library. */
 int gemm_version(void);
 
+/*
+ * C = A·B without allocating anything.  The pages have no counterpart of this
+ * entry point; it exists for callers that cannot call cudaMalloc: code whose
+ * device memory is owned by a framework's memory manager (every allocation
+ * must go through it, or the budget is reserved up front), and
+ * latency-critical threads that must not take cudaMalloc's implicit device
+ * synchronisation.  gemm_create and gemm_run allocate, so they are not usable
+ * there.
+ *
+ * Arguments, semantics, errors and asynchrony are those of gemm_run, without
+ * the handle: the call runs on the calling thread's current device, and
+ * `stream` must belong to that device.  Operands whose address or pitch is
+ * not a multiple of 16 bytes are re-packed into a scratch array of
+ * GEMM_NOALLOC_SCRATCH_BYTES that the library reserves as a static device
+ * array on every GPU that loads it, until the process exits.  When the
+ * re-packed A and B together need more than that, the call returns
+ * GEMM_ERR_INVALID and launches nothing (aligned operands need no scratch and
+ * have no such limit).
+ *
+ * The first call on a device does a one-time set-up there (device check,
+ * kernel attributes, lookup of the scratch array's device address); make
+ * that first call before any stream capture.  All calls on a device share
+ * the scratch array and it keeps the last call's contents; nothing in it has
+ * to start at zero, because each call writes every element it reads.  Calls
+ * that overlap on the GPU (unordered streams, or several host threads) race
+ * on the array: order them.  There is no status word: an in-kernel wait that
+ * expires ends the kernel without a report (gemm_sync_status covers only
+ * handle-based calls).  The call makes no cudaMalloc, cudaFree or other
+ * allocating call.
+ */
+#define GEMM_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+int gemm_run_noalloc(int layout_b, int64_t M, int64_t N, int64_t K,
+                     const void *A, int64_t lda, const void *B, int64_t ldb,
+                     float *C, int64_t ldc, int dtype, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
