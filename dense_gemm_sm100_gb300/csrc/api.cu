@@ -27,6 +27,7 @@ struct gemm_ctx {
     int simt_group_m = 0;
     int tc_group_m = 0;
     int max_ctas = 0;
+    int simt_config = 0;  // 0: chosen per shape; else configuration index + 1
 };
 
 namespace {
@@ -241,21 +242,24 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
     const char *lay = layout_b == GEMM_B_ROW_MAJOR ? "rowB" : "colB";
     int rc;
     if (dtype == GEMM_F32) {
-        rc = encode_2d(h, &tmA, 4, A, K, M, lda, dg::kSimtBoxA[0], dg::kSimtBoxA[1]);
+        const int cfg = h->simt_config > 0 ? h->simt_config - 1
+                                           : dg::simt_pick_config(M, N, h->sm_count);
+        const dg::SimtTile t = dg::simt_tile(cfg, layout_b);
+        rc = encode_2d(h, &tmA, 4, A, K, M, lda, dg::kSimtBK, t.bm);
         if (rc) return rc;
         if (layout_b == GEMM_B_ROW_MAJOR)
-            rc = encode_2d(h, &tmB, 4, B, N, K, ldb, dg::kSimtBoxBRow[0], dg::kSimtBoxBRow[1]);
+            rc = encode_2d(h, &tmB, 4, B, N, K, ldb, 32, dg::kSimtBK);
         else
-            rc = encode_2d(h, &tmB, 4, B, K, N, ldb, dg::kSimtBoxBCol[0], dg::kSimtBoxBCol[1]);
+            rc = encode_2d(h, &tmB, 4, B, K, N, ldb, dg::kSimtBK, t.bn);
         if (rc) return rc;
-        const int tiles = static_cast<int>(((M + dg::kSimtBM - 1) / dg::kSimtBM) *
-                                           ((N + dg::kSimtBN - 1) / dg::kSimtBN));
-        lc.grid = dg::simt_grid(tiles, h->max_ctas > 0 ? h->max_ctas : h->sm_count);
+        const int64_t tiles = ((M + t.bm - 1) / t.bm) * ((N + t.bn - 1) / t.bn);
+        const int64_t cap = h->max_ctas > 0 ? h->max_ctas : int64_t{h->sm_count} * t.ctas_per_sm;
+        lc.grid = static_cast<int>(tiles < cap ? tiles : cap);
         lc.group_m = h->simt_group_m;
-        cudaError_t e = dg::launch_simt_f32(tmA, tmB, layout_b, static_cast<int>(M), static_cast<int>(N),
+        cudaError_t e = dg::launch_simt_f32(cfg, tmA, tmB, layout_b, static_cast<int>(M), static_cast<int>(N),
                                             static_cast<int>(K), C, ldc, c_vec4, lc);
         if (e != cudaSuccess) return cuda_fail(h, e, "FP32 SIMT kernel launch");
-        path = std::string("simt_f32_128x128_") + lay + path;
+        path = std::string("simt_f32_") + t.name + "_" + lay + path;
     } else {
         const int bk = dg::tc_bk(es);
         rc = encode_2d(h, &tmA, es, A, K, M, lda, bk, dg::kTcBM);
@@ -468,8 +472,12 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value)
         h->tc_group_m = static_cast<int>(value);
         return GEMM_OK;
     case GEMM_OPT_MAX_CTAS:
-        if (value < 0 || value > h->sm_count) break;
+        if (value < 0 || value > 4 * int64_t{h->sm_count}) break;
         h->max_ctas = static_cast<int>(value);
+        return GEMM_OK;
+    case GEMM_OPT_SIMT_CONFIG:
+        if (value < 0 || value > dg::simt_num_configs()) break;
+        h->simt_config = static_cast<int>(value);
         return GEMM_OK;
     default:
         return fail(h, GEMM_ERR_INVALID, "unknown option");

@@ -7,15 +7,22 @@
 
 namespace dg {
 
-// Geometry of the FP32 SIMT kernel (sgemm_simt.cu).  A tile of C is
-// kSimtBM x kSimtBN; K advances kSimtBK elements (128 bytes) per stage.
-constexpr int kSimtBM = 128;
-constexpr int kSimtBN = 128;
+// The FP32 SIMT kernel (sgemm_simt.cu) comes in several tile configurations.
+// K advances kSimtBK elements (128 bytes) per stage in all of them.  TMA boxes
+// (innermost dimension first): A {kSimtBK, bm}; row-major B {32, kSimtBK}
+// repeated bn/32 times; column-major B {kSimtBK, bn}.
 constexpr int kSimtBK = 32;
-// TMA boxes, innermost dimension first.
-constexpr int kSimtBoxA[2] = {kSimtBK, kSimtBM};        // A rows, K contiguous
-constexpr int kSimtBoxBRow[2] = {32, kSimtBK};          // row-major B: 32 columns x BK rows
-constexpr int kSimtBoxBCol[2] = {kSimtBK, kSimtBN};     // column-major B: BN columns, K contiguous
+
+struct SimtTile {
+    int bm, bn;        // C tile of the configuration for the given B layout
+    int ctas_per_sm;   // resident CTAs per SM (persistent grid = SMs x this)
+    const char *name;
+};
+
+int simt_num_configs();
+SimtTile simt_tile(int config, int layout_b);
+// Configuration for an M x N problem on a GPU with sm_count SMs.
+int simt_pick_config(int64_t M, int64_t N, int sm_count);
 
 // Geometry of the tensor-core kernel (gemm_tc.cu).  A tile of C is
 // kTcBM x kTcBN; every stage holds 128 bytes of K per operand row, i.e.
@@ -37,11 +44,11 @@ struct LaunchCommon {
 cudaError_t prepare_simt();
 cudaError_t prepare_tc();
 
-// FP32 SIMT GEMM.  tmA maps A (dims {K, M}), tmB maps the stored B
-// (row-major: dims {N, K}; column-major: dims {K, N}), both FP32 with a
-// 128-byte swizzle and the boxes above.
-cudaError_t launch_simt_f32(const CUtensorMap &tmA, const CUtensorMap &tmB, int layout_b,
-                            int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
+// FP32 SIMT GEMM with configuration `config`.  tmA maps A (dims {K, M}),
+// tmB maps the stored B (row-major: dims {N, K}; column-major: dims {K, N}),
+// both FP32 with a 128-byte swizzle and the boxes of simt_tile(config).
+cudaError_t launch_simt_f32(int config, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                            int layout_b, int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
                             const LaunchCommon &lc);
 
 // Tensor-core GEMM; dtype is GEMM_TF32 or GEMM_BF16.  tmA/tmB as above with
@@ -58,8 +65,7 @@ cudaError_t launch_repack(const void *src, int64_t lds, void *dst, int64_t ldd, 
 cudaError_t launch_zero_fill(float *C, int64_t ldc, int64_t M, int64_t N, int sm_count,
                              cudaStream_t stream);
 
-// Persistent-grid size a kernel wants for `tiles` output tiles.
-int simt_grid(int tiles, int sm_count);
+// Persistent-grid size the tensor-core kernel wants for `tiles` output tiles.
 int tc_grid(int tiles, int sm_count);
 
 }  // namespace dg

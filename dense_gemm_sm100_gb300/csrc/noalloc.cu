@@ -156,18 +156,17 @@ extern "C" int gemm_run_noalloc(int layout_b, int64_t M, int64_t N, int64_t K, c
     const bool c_vec4 = reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 4 == 0;
     cudaError_t e;
     if (dtype == GEMM_F32) {
-        bool ok = encode(&tmA, 4, A, K, M, lda_p, dg::kSimtBoxA[0], dg::kSimtBoxA[1],
-                         CU_TENSOR_MAP_SWIZZLE_128B);
+        const int cfg = dg::simt_pick_config(M, N, s->sm_count);
+        const dg::SimtTile t = dg::simt_tile(cfg, layout_b);
+        bool ok = encode(&tmA, 4, A, K, M, lda_p, dg::kSimtBK, t.bm, CU_TENSOR_MAP_SWIZZLE_128B);
         ok = ok && (layout_b == GEMM_B_ROW_MAJOR
-                        ? encode(&tmB, 4, B, N, K, ldb_p, dg::kSimtBoxBRow[0], dg::kSimtBoxBRow[1],
-                                 CU_TENSOR_MAP_SWIZZLE_128B)
-                        : encode(&tmB, 4, B, K, N, ldb_p, dg::kSimtBoxBCol[0], dg::kSimtBoxBCol[1],
-                                 CU_TENSOR_MAP_SWIZZLE_128B));
+                        ? encode(&tmB, 4, B, N, K, ldb_p, 32, dg::kSimtBK, CU_TENSOR_MAP_SWIZZLE_128B)
+                        : encode(&tmB, 4, B, K, N, ldb_p, dg::kSimtBK, t.bn, CU_TENSOR_MAP_SWIZZLE_128B));
         if (!ok) return GEMM_ERR_CUDA;
-        const int tiles = static_cast<int>(((M + dg::kSimtBM - 1) / dg::kSimtBM) *
-                                           ((N + dg::kSimtBN - 1) / dg::kSimtBN));
-        lc.grid = dg::simt_grid(tiles, s->sm_count);
-        e = dg::launch_simt_f32(tmA, tmB, layout_b, static_cast<int>(M), static_cast<int>(N),
+        const int64_t tiles = ((M + t.bm - 1) / t.bm) * ((N + t.bn - 1) / t.bn);
+        const int64_t cap = int64_t{s->sm_count} * t.ctas_per_sm;
+        lc.grid = static_cast<int>(tiles < cap ? tiles : cap);
+        e = dg::launch_simt_f32(cfg, tmA, tmB, layout_b, static_cast<int>(M), static_cast<int>(N),
                                 static_cast<int>(K), C, ldc, c_vec4, lc);
     } else {
         const int bk = dg::tc_bk(es);

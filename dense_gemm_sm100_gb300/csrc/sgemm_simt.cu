@@ -3,25 +3,25 @@
 //
 // Design, restating the optimisation steps of "GEMM 性能优化" (八个台阶) for
 // Blackwell:
-//  * 台阶 1 (shared-memory tiling along K): each CTA owns a 128x128 tile of C
+//  * 台阶 1 (shared-memory tiling along K): each CTA owns a BM x BN tile of C
 //    and walks K in 32-element slices staged in shared memory.
-//  * 台阶 2 (thread tiling): every consumer thread keeps an 8x8 block of C in
-//    registers and does 64 FMAs per k from 8 A and 8 B values.
+//  * 台阶 2 (thread tiling): every consumer thread keeps an 8 x TN block of C
+//    in registers and does 8*TN FMAs per k from 8 A and TN B values.
 //  * 台阶 3/4 (vector loads, bank conflicts): the Tensor Memory Accelerator
 //    writes each stage with a 128-byte XOR swizzle; every shared load is a
 //    16-byte vector and the thread-to-data mapping below makes each warp-wide
 //    load hit 32 distinct banks (or broadcast).
-//  * 台阶 5 (warp tiling): a warp covers 64 rows x 64 columns of the tile
-//    through 4x8 lanes; lanes that share a row group share A loads.
+//  * 台阶 5 (warp tiling): a warp is 4 x 8 lanes covering 32 rows x 8*TN
+//    columns; lanes that share a row group share A loads.
 //  * 台阶 6/7 (double buffering, asynchronous copies): a dedicated producer
-//    warp issues TMA copies into a 6-stage ring guarded by mbarriers, so
-//    global loads overlap the math; register fragments of the next k group
-//    are loaded while the current one is multiplied.
+//    warp issues TMA copies into a multi-stage ring guarded by mbarriers, so
+//    global loads overlap the math; fragments of the next k group are loaded
+//    while the current one is multiplied.
 //  * 台阶 8 (SASS tuning) is replaced by source-level structure: compile-time
-//    power-of-two tiles, offsets precomputed per thread so every shared load
-//    is base + immediate, and __launch_bounds__.
-//  * Wave model / block order: the grid is persistent (one CTA per SM) and
-//    walks tiles in groups of `group_m` tile rows for L2 reuse.
+//    power-of-two tiles, swizzled offsets computed once per thread, and
+//    __launch_bounds__.
+//  * Wave model / block order: the grid is persistent and walks tiles in
+//    groups of `group_m` tile rows for L2 reuse.
 //  * Column-major B ("PMPP Chapter 06: Performance considerations", section
 //    1, corner turning): TMA reads B along its contiguous K direction
 //    (coalesced), and the transposed access happens in shared memory.
@@ -36,18 +36,7 @@
 namespace dg {
 namespace {
 
-constexpr int BM = kSimtBM, BN = kSimtBN, BK = kSimtBK;
-constexpr int STAGES = 6;
-constexpr int A_BYTES = BM * BK * 4;  // 16 KiB
-constexpr int B_BYTES = BK * BN * 4;  // 16 KiB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int CONSUMER_WARPS = 8;
-constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;
-constexpr int BAR_BYTES = 2 * STAGES * 8 + 16;
-constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + BAR_BYTES;
-
-static_assert(BM == 128 && BN == 128 && BK == 32, "thread mapping assumes 128x128x32 tiles");
-static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+constexpr int BK = kSimtBK;  // 32 FP32 = one 128-byte swizzle row
 
 struct SimtParams {
     int M, N, K;
@@ -72,11 +61,40 @@ __device__ __forceinline__ void tile_coords(int t, const SimtParams &p, int &mb,
     nb = r / gm;
 }
 
-template <int LAYOUT_B>
-__global__ void __launch_bounds__(THREADS, 1)
+// WM x WN consumer warps; a thread owns 8 rows x TN columns of C; STAGES ring
+// slots; GU k-groups (4 k each) per unrolled inner iteration (8 = a whole
+// stage); F2 = 1 issues the multiply-adds of row-major B as packed pairs
+// (fma.rn.f32x2: two independent FP32 FMAs per instruction, same rounding, so
+// the same bits), halving the FMA instructions the scheduler has to issue.
+// Column-major B keeps scalar FMAs: its B pairs would have to be assembled
+// from two fragments, which costs more issue slots than the packing saves.
+template <int LAYOUT_B, int WM, int WN, int TN, int STAGES, int GU, int F2>
+struct Simt {
+    static_assert(WM % 2 == 0, "row interleave pairs warps along M");
+    static_assert(TN % 4 == 0 && TN <= 16, "thread tile width");
+    static_assert(LAYOUT_B == 0 || TN <= 8, "column-major B uses at most 8 columns per thread");
+    static_assert(8 % GU == 0, "k groups per iteration");
+    static constexpr int BM = WM * 32;
+    static constexpr int BN = WN * 8 * TN;
+    static constexpr int A_BYTES = BM * 128;
+    static constexpr int B_BYTES = BN * 128;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int CONSUMER_WARPS = WM * WN;
+    static constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 2 * STAGES * 8 + 16;
+    static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+    static_assert(BM <= 256 && BN <= 256, "TMA box limit");
+};
+
+template <int LAYOUT_B, int WM, int WN, int TN, int STAGES, int GU, int F2>
+__global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>::THREADS, 1)
     sgemm_simt_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const SimtParams p)
 {
+    using S = Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>;
+    constexpr int BM = S::BM, BN = S::BN, A_BYTES = S::A_BYTES, STAGE_BYTES = S::STAGE_BYTES;
+    constexpr int CONSUMER_WARPS = S::CONSUMER_WARPS;
+
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t pad = ((raw_addr + 1023u) & ~1023u) - raw_addr;
@@ -84,7 +102,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t sbase = raw_addr + pad;
     const uint32_t full_bar = sbase + STAGES * STAGE_BYTES;  // STAGES x 8 bytes
     const uint32_t empty_bar = full_bar + STAGES * 8;         // STAGES x 8 bytes
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + STAGES * STAGE_BYTES + 2 * STAGES * 8);
+    volatile int *abort_flag =
+        reinterpret_cast<volatile int *>(smem + STAGES * STAGE_BYTES + 2 * STAGES * 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -145,38 +164,32 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 
     // ---------------------------------------------------------- consumers
-    const int wm = warp >> 1;  // 0..3
-    const int wn = warp & 1;   // 0..1
+    const int wm = warp % WM;
+    const int wn = warp / WM;
     const int lr = lane >> 3;  // 0..3
     const int lc = lane & 7;   // 0..7
     // Rows row0 + 8*i (i < 8): the two warps of a 64-row band interleave by
     // four rows, so row & 7 is fixed per thread and distinct across the four
     // row groups of a warp (conflict-free swizzled A loads).
     const int row0 = (wm >> 1) * 64 + (wm & 1) * 4 + lr;
-    uint32_t a_off[8], b_off[8];
-#pragma unroll
-    for (int g = 0; g < 8; ++g) a_off[g] = row0 * 128 + ((g ^ (row0 & 7)) << 4);
-    if (LAYOUT_B == 0) {
-        // Columns wn*64 + 4*lc + {0..3} and +32: chunk lc of boxes 2wn and
-        // 2wn+1; b_off[c] serves every k with k & 7 == c.
-#pragma unroll
-        for (int c = 0; c < 8; ++c) b_off[c] = A_BYTES + (2 * wn) * 4096 + ((lc ^ c) << 4);
-    } else {
-        // Columns col0 + 8*j: col0 & 7 == lc, distinct across the warp.
-        const int col0 = wn * 64 + lc;
-#pragma unroll
-        for (int g = 0; g < 8; ++g) b_off[g] = A_BYTES + col0 * 128 + ((g ^ lc) << 4);
-    }
+    const uint32_t xa = row0 & 7;
+    const uint32_t a_base = row0 * 128;
+    // Row-major B: columns wn*8*TN + 32*c + 4*lc + {0..3} (c < TN/4), i.e.
+    // chunk lc of box wn*TN/4 + c; the chunk's place in row k is lc ^ (k & 7).
+    // Column-major B: columns col0 + 8*j with col0 & 7 == lc.
+    const int col0 = LAYOUT_B == 0 ? wn * 8 * TN + 4 * lc : wn * 8 * TN + lc;
+    const uint32_t b_base = LAYOUT_B == 0 ? A_BYTES + wn * (TN / 4) * 4096 : A_BYTES + col0 * 128;
 
     uint32_t it = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
         int mb, nb;
         tile_coords(tile, p, mb, nb);
-        float acc[8][8];
+        // acc2[i][jp] holds columns 2*jp and 2*jp + 1 of row i.
+        float2 acc2[8][TN / 2];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+            for (int j = 0; j < TN / 2; ++j) acc2[i][j] = make_float2(0.0f, 0.0f);
 
         for (int kt = 0; kt < k_tiles; ++kt, ++it) {
             const uint32_t s = it % STAGES;
@@ -185,41 +198,55 @@ __global__ void __launch_bounds__(THREADS, 1)
                            p.timeout_ns))
                 return;
             const uint8_t *st = smem + s * STAGE_BYTES;
+#pragma unroll 1
+            for (int g0 = 0; g0 < 8; g0 += GU) {
 #pragma unroll
-            for (int g = 0; g < BK / 4; ++g) {
-                float4 a[8];
+                for (int h = 0; h < GU; ++h) {
+                    const int g = g0 + h;
+                    const uint8_t *ap = st + a_base + ((g ^ xa) << 4);
+                    float4 a[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    a[i] = *reinterpret_cast<const float4 *>(st + a_off[g] + i * 1024);
-                if (LAYOUT_B == 0) {
+                    for (int i = 0; i < 8; ++i) a[i] = *reinterpret_cast<const float4 *>(ap + i * 1024);
+                    float4 bcol[LAYOUT_B == 0 ? 1 : TN];
+                    if (LAYOUT_B != 0) {
+                        const uint8_t *bp = st + b_base + ((g ^ lc) << 4);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const int k = 4 * g + kk;
-                        const uint8_t *bp = st + b_off[k & 7] + k * 128;
-                        const float4 b0 = *reinterpret_cast<const float4 *>(bp);
-                        const float4 b1 = *reinterpret_cast<const float4 *>(bp + 4096);
-                        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av, bv[j], acc[i][j]);
-                        }
+                        for (int j = 0; j < TN; ++j) bcol[j] = *reinterpret_cast<const float4 *>(bp + j * 1024);
                     }
-                } else {
-                    float4 b[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        b[j] = *reinterpret_cast<const float4 *>(st + b_off[g] + j * 1024);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
+                        // b2[jp] = columns (2*jp, 2*jp + 1) of B row k = 4*g + kk.
+                        float2 b2[TN / 2];
+                        if (LAYOUT_B == 0) {
+                            const int k = 4 * g + kk;
+                            const uint8_t *bp = st + b_base + k * 128 + ((lc ^ (k & 7)) << 4);
+#pragma unroll
+                            for (int c = 0; c < TN / 4; ++c) {
+                                const float4 b4 = *reinterpret_cast<const float4 *>(bp + c * 4096);
+                                b2[2 * c] = make_float2(b4.x, b4.y);
+                                b2[2 * c + 1] = make_float2(b4.z, b4.w);
+                            }
+                        } else {
+#pragma unroll
+                            for (int jp = 0; jp < TN / 2; ++jp) {
+                                const float4 u = bcol[2 * jp], v = bcol[2 * jp + 1];
+                                b2[jp] = make_float2(kk == 0 ? u.x : kk == 1 ? u.y : kk == 2 ? u.z : u.w,
+                                                     kk == 0 ? v.x : kk == 1 ? v.y : kk == 2 ? v.z : v.w);
+                            }
+                        }
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+                            if (F2 && LAYOUT_B == 0) {
+                                const float2 aa = make_float2(av, av);
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                const float bv = kk == 0 ? b[j].x : kk == 1 ? b[j].y : kk == 2 ? b[j].z : b[j].w;
-                                acc[i][j] = fmaf(av, bv, acc[i][j]);
+                                for (int jp = 0; jp < TN / 2; ++jp) acc2[i][jp] = __ffma2_rn(aa, b2[jp], acc2[i][jp]);
+                            } else {
+#pragma unroll
+                                for (int jp = 0; jp < TN / 2; ++jp) {
+                                    acc2[i][jp].x = fmaf(av, b2[jp].x, acc2[i][jp].x);
+                                    acc2[i][jp].y = fmaf(av, b2[jp].y, acc2[i][jp].y);
+                                }
                             }
                         }
                     }
@@ -231,82 +258,151 @@ __global__ void __launch_bounds__(THREADS, 1)
 
         // ------------------------------------------------------ epilogue
         const long long m_base = (long long)mb * BM + row0;
-        if (LAYOUT_B == 0) {
-            const int n_base = nb * BN + wn * 64 + 4 * lc;
+        const int n_base = nb * BN + col0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const long long m = m_base + 8 * i;
-                if (m >= p.M) continue;
-                float *crow = p.C + m * p.ldc;
+        for (int i = 0; i < 8; ++i) {
+            const long long m = m_base + 8 * i;
+            if (m >= p.M) continue;
+            float *crow = p.C + m * p.ldc;
+            if (LAYOUT_B == 0) {
+                // columns 32*c + {0..3}: pairs 2c and 2c + 1
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int n = n_base + 32 * h;
+                for (int c = 0; c < TN / 4; ++c) {
+                    const int n = n_base + 32 * c;
+                    const float2 lo = acc2[i][2 * c], hi = acc2[i][2 * c + 1];
                     if (p.c_vec4 && n + 3 < p.N) {
-                        *reinterpret_cast<float4 *>(crow + n) =
-                            make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
+                        *reinterpret_cast<float4 *>(crow + n) = make_float4(lo.x, lo.y, hi.x, hi.y);
                     } else {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            if (n + q < p.N) crow[n + q] = acc[i][4 * h + q];
+                        if (n < p.N) crow[n] = lo.x;
+                        if (n + 1 < p.N) crow[n + 1] = lo.y;
+                        if (n + 2 < p.N) crow[n + 2] = hi.x;
+                        if (n + 3 < p.N) crow[n + 3] = hi.y;
                     }
                 }
-            }
-        } else {
-            const int n_base = nb * BN + wn * 64 + lc;
+            } else {
+                // column col0 + 8*j is element j & 1 of pair j / 2
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const long long m = m_base + 8 * i;
-                if (m >= p.M) continue;
-                float *crow = p.C + m * p.ldc;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < TN; ++j) {
                     const int n = n_base + 8 * j;
-                    if (n < p.N) crow[n] = acc[i][j];
+                    if (n < p.N) crow[n] = (j & 1) ? acc2[i][j / 2].y : acc2[i][j / 2].x;
                 }
             }
         }
     }
 }
 
-template <int L>
-cudaError_t set_attrs()
+// ------------------------------------------------------------------ configs
+
+struct ConfigEntry {
+    int bm, bn_row, bn_col, ctas_per_sm;
+    const char *name;
+    cudaError_t (*prepare)(int *ctas_per_sm);
+    void (*launch)(int layout_b, const CUtensorMap &, const CUtensorMap &, const SimtParams &,
+                   int grid, cudaStream_t);
+};
+
+template <int L, int WM, int WN, int TN, int ST, int GU, int F2>
+cudaError_t prepare_one(int *ctas)
 {
-    return cudaFuncSetAttribute(sgemm_simt_kernel<L>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                SMEM_BYTES);
+    using S = Simt<L, WM, WN, TN, ST, GU, F2>;
+    auto k = sgemm_simt_kernel<L, WM, WN, TN, ST, GU, F2>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, k, S::THREADS, S::SMEM_BYTES);
+    return e;
 }
+
+// Row-major B runs the table's TN; column-major B runs min(TN, 8).
+constexpr int col_tn(int tn) { return tn < 8 ? tn : 8; }
+
+template <int WM, int WN, int TN, int ST, int GU, int F2>
+cudaError_t prepare_cfg(int *ctas)
+{
+    int c0 = 0, c1 = 0;
+    cudaError_t e = prepare_one<0, WM, WN, TN, ST, GU, F2>(&c0);
+    if (e == cudaSuccess) e = prepare_one<1, WM, WN, col_tn(TN), ST, GU, F2>(&c1);
+    *ctas = c0 < c1 ? c0 : c1;
+    return e;
+}
+
+template <int WM, int WN, int TN, int ST, int GU, int F2>
+void launch_cfg(int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB, const SimtParams &p,
+                int grid, cudaStream_t stream)
+{
+    if (layout_b == 0) {
+        using S = Simt<0, WM, WN, TN, ST, GU, F2>;
+        sgemm_simt_kernel<0, WM, WN, TN, ST, GU, F2><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
+    } else {
+        using S = Simt<1, WM, WN, col_tn(TN), ST, GU, F2>;
+        sgemm_simt_kernel<1, WM, WN, col_tn(TN), ST, GU, F2><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
+    }
+}
+
+#define DG_SIMT_CFG(WM, WN, TN, ST, GU, F2, NAME)                                              \
+    {WM * 32, WN * 8 * TN, WN * 8 * col_tn(TN), 0, NAME, prepare_cfg<WM, WN, TN, ST, GU, F2>,  \
+     launch_cfg<WM, WN, TN, ST, GU, F2>}
+
+// Config table; GEMM_OPT_SIMT_CONFIG selects entry (value - 1).
+ConfigEntry g_configs[] = {
+    DG_SIMT_CFG(4, 2, 8, 6, 8, 1, "128x128"),
+    DG_SIMT_CFG(4, 2, 8, 6, 8, 0, "128x128s"),
+    DG_SIMT_CFG(4, 2, 16, 4, 8, 1, "128x256"),
+    DG_SIMT_CFG(4, 4, 4, 6, 8, 1, "128x128w16"),
+    DG_SIMT_CFG(2, 2, 8, 4, 8, 1, "64x128"),
+    DG_SIMT_CFG(2, 1, 8, 4, 8, 1, "64x64"),
+};
+constexpr int kNumConfigs = sizeof(g_configs) / sizeof(g_configs[0]);
 
 }  // namespace
 
 cudaError_t prepare_simt()
 {
-    cudaError_t e = set_attrs<0>();
-    if (e == cudaSuccess) e = set_attrs<1>();
-    return e;
+    for (int i = 0; i < kNumConfigs; ++i) {
+        int ctas = 0;
+        cudaError_t e = g_configs[i].prepare(&ctas);
+        if (e != cudaSuccess) return e;
+        g_configs[i].ctas_per_sm = ctas > 0 ? ctas : 1;
+    }
+    return cudaSuccess;
 }
 
-int simt_grid(int tiles, int sm_count) { return tiles < sm_count ? tiles : sm_count; }
+int simt_num_configs() { return kNumConfigs; }
 
-cudaError_t launch_simt_f32(const CUtensorMap &tmA, const CUtensorMap &tmB, int layout_b, int M,
-                            int N, int K, float *C, int64_t ldc, bool c_vec4,
+SimtTile simt_tile(int config, int layout_b)
+{
+    const ConfigEntry &c = g_configs[config];
+    return SimtTile{c.bm, layout_b == 0 ? c.bn_row : c.bn_col, c.ctas_per_sm, c.name};
+}
+
+int simt_pick_config(int64_t M, int64_t N, int sm_count)
+{
+    // The 128x128 tile when it gives every SM a tile; else smaller tiles, so
+    // small problems still spread over the GPU (wave model).
+    const int64_t t128 = ((M + 127) / 128) * ((N + 127) / 128);
+    if (t128 >= sm_count) return 0;
+    const int64_t t64x128 = ((M + 63) / 64) * ((N + 127) / 128);
+    if (t64x128 >= sm_count) return 4;
+    return 5;
+}
+
+cudaError_t launch_simt_f32(int config, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                            int layout_b, int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
                             const LaunchCommon &lc)
 {
+    const SimtTile t = simt_tile(config, layout_b);
     SimtParams p;
     p.M = M;
     p.N = N;
     p.K = K;
-    p.tiles_m = (M + BM - 1) / BM;
-    p.tiles_n = (N + BN - 1) / BN;
+    p.tiles_m = (M + t.bm - 1) / t.bm;
+    p.tiles_n = (N + t.bn - 1) / t.bn;
     p.group_m = lc.group_m > 0 ? lc.group_m : 8;
     p.C = C;
     p.ldc = ldc;
     p.status = lc.status;
     p.timeout_ns = lc.timeout_ns;
     p.c_vec4 = c_vec4 ? 1 : 0;
-    const dim3 grid(lc.grid), block(THREADS);
-    if (layout_b == 0)
-        sgemm_simt_kernel<0><<<grid, block, SMEM_BYTES, lc.stream>>>(tmA, tmB, p);
-    else
-        sgemm_simt_kernel<1><<<grid, block, SMEM_BYTES, lc.stream>>>(tmA, tmB, p);
+    g_configs[config].launch(layout_b, tmA, tmB, p, lc.grid, lc.stream);
     return cudaGetLastError();
 }
 

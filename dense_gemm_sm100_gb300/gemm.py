@@ -37,6 +37,7 @@ GEMM_OPT_WAIT_TIMEOUT_NS = 2
 GEMM_OPT_SIMT_GROUP_M = 3
 GEMM_OPT_TC_GROUP_M = 4
 GEMM_OPT_MAX_CTAS = 5
+GEMM_OPT_SIMT_CONFIG = 6
 
 DTYPES = {"f32": GEMM_F32, "tf32": GEMM_TF32, "bf16": GEMM_BF16}
 LAYOUTS = {"row": GEMM_B_ROW_MAJOR, "col": GEMM_B_COL_MAJOR}

@@ -79,7 +79,8 @@ extern "C" {
 #define GEMM_OPT_WAIT_TIMEOUT_NS 2 /* limit of every in-kernel wait, nanoseconds (default 4e9) */
 #define GEMM_OPT_SIMT_GROUP_M 3   /* tile-order group height in tiles for the FP32 kernel */
 #define GEMM_OPT_TC_GROUP_M 4     /* tile-order group height in tiles for the tensor-core kernel */
-#define GEMM_OPT_MAX_CTAS 5       /* cap on persistent CTAs (0 = one per SM) */
+#define GEMM_OPT_MAX_CTAS 5       /* cap on persistent CTAs (0 = SMs x resident CTAs per SM) */
+#define GEMM_OPT_SIMT_CONFIG 6    /* FP32 tile configuration: 0 = chosen per shape, else 1..6 */
 
 typedef struct gemm_ctx *gemm_handle_t;
 
