@@ -28,6 +28,7 @@ struct gemm_ctx {
     int tc_group_m = 0;
     int max_ctas = 0;
     int simt_config = 0;  // 0: chosen per shape; else configuration index + 1
+    int split_k = 0;      // 0: chosen per shape; 1: never; n > 1: n K slices (FP32 path)
 };
 
 namespace {
@@ -102,12 +103,16 @@ bool tma_ready(const void *p, int64_t ld, int es)
     return reinterpret_cast<uintptr_t>(p) % 16 == 0 && (ld * es) % 16 == 0;
 }
 
-// Bytes of workspace the operand re-pack needs (0 when both are TMA-ready).
+// Workspace a run needs: re-packed operands (when not TMA-ready) followed by
+// the split-K partial products of the FP32 path.
 struct PackPlan {
     bool a = false, b = false;
     int64_t lda = 0, ldb = 0;
     size_t a_bytes = 0, b_bytes = 0;
-    size_t total() const { return a_bytes + b_bytes; }
+    int simt_config = 0;
+    dg::SplitK split;     // partials pointer is filled in by run_device
+    size_t split_bytes = 0;
+    size_t total() const { return a_bytes + b_bytes + split_bytes; }
 };
 
 PackPlan plan_pack(const gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K,
@@ -128,6 +133,20 @@ PackPlan plan_pack(const gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_
         const int64_t cols = layout_b == GEMM_B_ROW_MAJOR ? N : K;
         pp.ldb = round_up(cols, align_elems);
         pp.b_bytes = static_cast<size_t>(round_up(rows * pp.ldb * es, 256));
+    }
+    if (dtype == GEMM_F32) {
+        pp.simt_config = h->simt_config > 0 ? h->simt_config - 1 : dg::simt_pick_config(M, N, h->sm_count);
+        if (h->split_k == 0) {
+            pp.split = dg::simt_pick_splits(pp.simt_config, layout_b, M, N, K, h->sm_count);
+        } else if (h->split_k > 1) {
+            const int64_t k_tiles = (K + dg::kSimtBK - 1) / dg::kSimtBK;
+            const int64_t want = h->split_k < k_tiles ? h->split_k : k_tiles;
+            const int64_t kt_per = (k_tiles + want - 1) / want;
+            pp.split.splits = static_cast<int>((k_tiles + kt_per - 1) / kt_per);
+            pp.split.k_per_split = static_cast<int>(kt_per * dg::kSimtBK);
+        }
+        if (pp.split.splits > 1)
+            pp.split_bytes = static_cast<size_t>(round_up(int64_t{pp.split.splits} * M * N * 4, 256));
     }
     return pp;
 }
@@ -242,8 +261,7 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
     const char *lay = layout_b == GEMM_B_ROW_MAJOR ? "rowB" : "colB";
     int rc;
     if (dtype == GEMM_F32) {
-        const int cfg = h->simt_config > 0 ? h->simt_config - 1
-                                           : dg::simt_pick_config(M, N, h->sm_count);
+        const int cfg = pp.simt_config;
         const dg::SimtTile t = dg::simt_tile(cfg, layout_b);
         rc = encode_2d(h, &tmA, 4, A, K, M, lda, dg::kSimtBK, t.bm);
         if (rc) return rc;
@@ -252,14 +270,22 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
         else
             rc = encode_2d(h, &tmB, 4, B, K, N, ldb, dg::kSimtBK, t.bn);
         if (rc) return rc;
-        const int64_t tiles = ((M + t.bm - 1) / t.bm) * ((N + t.bn - 1) / t.bn);
+        dg::SplitK sk = pp.split;
+        if (sk.splits > 1) sk.partials = reinterpret_cast<float *>(ws + pp.a_bytes + pp.b_bytes);
+        const int64_t units = ((M + t.bm - 1) / t.bm) * ((N + t.bn - 1) / t.bn) * sk.splits;
         const int64_t cap = h->max_ctas > 0 ? h->max_ctas : int64_t{h->sm_count} * t.ctas_per_sm;
-        lc.grid = static_cast<int>(tiles < cap ? tiles : cap);
+        lc.grid = static_cast<int>(units < cap ? units : cap);
         lc.group_m = h->simt_group_m;
         cudaError_t e = dg::launch_simt_f32(cfg, tmA, tmB, layout_b, static_cast<int>(M), static_cast<int>(N),
-                                            static_cast<int>(K), C, ldc, c_vec4, lc);
+                                            static_cast<int>(K), C, ldc, c_vec4, lc, sk);
         if (e != cudaSuccess) return cuda_fail(h, e, "FP32 SIMT kernel launch");
         path = std::string("simt_f32_") + t.name + "_" + lay + path;
+        if (sk.splits > 1) {
+            ++h->launches;
+            e = dg::launch_splitk_reduce(sk.partials, sk.splits, C, ldc, M, N, h->sm_count, stream);
+            if (e != cudaSuccess) return cuda_fail(h, e, "split-K reduction launch");
+            path += "+splitk" + std::to_string(sk.splits);
+        }
     } else {
         const int bk = dg::tc_bk(es);
         rc = encode_2d(h, &tmA, es, A, K, M, lda, bk, dg::kTcBM);
@@ -478,6 +504,10 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value)
     case GEMM_OPT_SIMT_CONFIG:
         if (value < 0 || value > dg::simt_num_configs()) break;
         h->simt_config = static_cast<int>(value);
+        return GEMM_OK;
+    case GEMM_OPT_SPLIT_K:
+        if (value < 0 || value > 64) break;
+        h->split_k = static_cast<int>(value);
         return GEMM_OK;
     default:
         return fail(h, GEMM_ERR_INVALID, "unknown option");

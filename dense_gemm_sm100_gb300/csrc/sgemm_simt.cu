@@ -41,11 +41,19 @@ constexpr int BK = kSimtBK;  // 32 FP32 = one 128-byte swizzle row
 struct SimtParams {
     int M, N, K;
     int tiles_m, tiles_n, group_m;
+    int splits;          // K slices per tile (1 = no split)
+    int k_per_split;     // elements of K per slice, a multiple of BK
     float *C;
     long long ldc;
+    long long split_stride;  // elements between the partial-C slices
     int *status;
     unsigned long long timeout_ns;
     int c_vec4;
+};
+
+// Work unit u (persistent loop index) -> output tile and K slice.
+struct Unit {
+    int mb, nb, kt_begin, kt_end, split;
 };
 
 // Tile t of the grouped order: groups of `group_m` tile rows, column-major
@@ -59,6 +67,22 @@ __device__ __forceinline__ void tile_coords(int t, const SimtParams &p, int &mb,
     const int r = t - g * per_group;
     mb = first_m + r % gm;
     nb = r / gm;
+}
+
+// Units run slice-major: unit u is tile u % tiles of K slice u / tiles.  The
+// K range of slice s is [s*k_per_split, min(K, (s+1)*k_per_split)) ("GEMM
+// 性能优化", 台阶 1: partial sums over K slices add up to the product).
+__device__ __forceinline__ Unit unit_coords(int u, const SimtParams &p)
+{
+    const int tiles = p.tiles_m * p.tiles_n;
+    Unit w;
+    w.split = u / tiles;
+    tile_coords(u - w.split * tiles, p, w.mb, w.nb);
+    const int k0 = w.split * p.k_per_split;
+    const int k1 = min(p.K, k0 + p.k_per_split);
+    w.kt_begin = k0 / kSimtBK;
+    w.kt_end = (k1 + kSimtBK - 1) / kSimtBK;
+    return w;
 }
 
 // WM x WN consumer warps; a thread owns 8 rows x TN columns of C; STAGES ring
@@ -107,8 +131,7 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>::TH
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int num_tiles = p.tiles_m * p.tiles_n;
-    const int k_tiles = (p.K + BK - 1) / BK;
+    const int num_units = p.tiles_m * p.tiles_n * p.splits;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -127,10 +150,10 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>::TH
         tma_prefetch_desc(&tmB);
         uint32_t it = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-            int mb, nb;
-            tile_coords(tile, p, mb, nb);
-            for (int kt = 0; kt < k_tiles; ++kt, ++it) {
+        for (int unit = blockIdx.x; ok && unit < num_units; unit += gridDim.x) {
+            const Unit w = unit_coords(unit, p);
+            const int mb = w.mb, nb = w.nb;
+            for (int kt = w.kt_begin; kt < w.kt_end; ++kt, ++it) {
                 const uint32_t s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1u;
                 if (!mbar_wait(empty_bar + 8 * s, ph ^ 1u, abort_flag, p.status,
@@ -181,9 +204,9 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>::TH
     const uint32_t b_base = LAYOUT_B == 0 ? A_BYTES + wn * (TN / 4) * 4096 : A_BYTES + col0 * 128;
 
     uint32_t it = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-        int mb, nb;
-        tile_coords(tile, p, mb, nb);
+    for (int unit = blockIdx.x; unit < num_units; unit += gridDim.x) {
+        const Unit w = unit_coords(unit, p);
+        const int mb = w.mb, nb = w.nb;
         // acc2[i][jp] holds columns 2*jp and 2*jp + 1 of row i.
         float2 acc2[8][TN / 2];
 #pragma unroll
@@ -191,7 +214,7 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>::TH
 #pragma unroll
             for (int j = 0; j < TN / 2; ++j) acc2[i][j] = make_float2(0.0f, 0.0f);
 
-        for (int kt = 0; kt < k_tiles; ++kt, ++it) {
+        for (int kt = w.kt_begin; kt < w.kt_end; ++kt, ++it) {
             const uint32_t s = it % STAGES;
             const uint32_t ph = (it / STAGES) & 1u;
             if (!mbar_wait(full_bar + 8 * s, ph, abort_flag, p.status, kWaitConsumerFull,
@@ -257,13 +280,15 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>::TH
         }
 
         // ------------------------------------------------------ epilogue
+        // C itself, or the partial-sum slice of this unit's K range.
+        float *cbase = p.C + (long long)w.split * p.split_stride;
         const long long m_base = (long long)mb * BM + row0;
         const int n_base = nb * BN + col0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const long long m = m_base + 8 * i;
             if (m >= p.M) continue;
-            float *crow = p.C + m * p.ldc;
+            float *crow = cbase + m * p.ldc;
             if (LAYOUT_B == 0) {
                 // columns 32*c + {0..3}: pairs 2c and 2c + 1
 #pragma unroll
@@ -376,18 +401,40 @@ SimtTile simt_tile(int config, int layout_b)
 
 int simt_pick_config(int64_t M, int64_t N, int sm_count)
 {
-    // The 128x128 tile when it gives every SM a tile; else smaller tiles, so
-    // small problems still spread over the GPU (wave model).
-    const int64_t t128 = ((M + 127) / 128) * ((N + 127) / 128);
-    if (t128 >= sm_count) return 0;
-    const int64_t t64x128 = ((M + 63) / 64) * ((N + 127) / 128);
-    if (t64x128 >= sm_count) return 4;
-    return 5;
+    // The 128x128 tile everywhere: a smaller tile does not shorten a
+    // thread's serial chain of 64*K multiply-adds, which is what bounds an
+    // under-filled launch; split-K does (simt_pick_splits).
+    (void)M;
+    (void)N;
+    (void)sm_count;
+    return 0;
+}
+
+SplitK simt_pick_splits(int config, int layout_b, int64_t M, int64_t N, int64_t K, int sm_count)
+{
+    // Wave model ("GEMM 性能优化", Wave 模型): when the tiles fill less than one
+    // wave, cut K into slices so tiles x slices fill it, keeping at least
+    // four 32-element k-tiles per slice.
+    const SimtTile t = simt_tile(config, layout_b);
+    const int64_t tiles = ((M + t.bm - 1) / t.bm) * ((N + t.bn - 1) / t.bn);
+    const int64_t slots = int64_t{sm_count} * t.ctas_per_sm;
+    const int64_t k_tiles = (K + kSimtBK - 1) / kSimtBK;
+    int64_t s = tiles > 0 ? slots / tiles : 1;
+    s = s < k_tiles / 4 ? s : k_tiles / 4;
+    s = s < 16 ? s : 16;
+    SplitK sk;
+    sk.splits = s > 1 ? static_cast<int>(s) : 1;
+    if (sk.splits > 1) {
+        const int64_t kt_per = (k_tiles + sk.splits - 1) / sk.splits;
+        sk.k_per_split = static_cast<int>(kt_per * kSimtBK);
+        sk.splits = static_cast<int>((k_tiles + kt_per - 1) / kt_per);  // no empty slice
+    }
+    return sk;
 }
 
 cudaError_t launch_simt_f32(int config, const CUtensorMap &tmA, const CUtensorMap &tmB,
                             int layout_b, int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
-                            const LaunchCommon &lc)
+                            const LaunchCommon &lc, const SplitK &sk)
 {
     const SimtTile t = simt_tile(config, layout_b);
     SimtParams p;
@@ -397,11 +444,14 @@ cudaError_t launch_simt_f32(int config, const CUtensorMap &tmA, const CUtensorMa
     p.tiles_m = (M + t.bm - 1) / t.bm;
     p.tiles_n = (N + t.bn - 1) / t.bn;
     p.group_m = lc.group_m > 0 ? lc.group_m : 8;
-    p.C = C;
-    p.ldc = ldc;
+    p.splits = sk.splits > 1 ? sk.splits : 1;
+    p.k_per_split = p.splits > 1 ? sk.k_per_split : K;
+    p.C = p.splits > 1 ? sk.partials : C;
+    p.ldc = p.splits > 1 ? N : ldc;
+    p.split_stride = static_cast<long long>(M) * N;
     p.status = lc.status;
     p.timeout_ns = lc.timeout_ns;
-    p.c_vec4 = c_vec4 ? 1 : 0;
+    p.c_vec4 = p.splits > 1 ? (N % 4 == 0) : (c_vec4 ? 1 : 0);
     g_configs[config].launch(layout_b, tmA, tmB, p, lc.grid, lc.stream);
     return cudaGetLastError();
 }

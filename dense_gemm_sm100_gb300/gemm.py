@@ -38,6 +38,7 @@ GEMM_OPT_SIMT_GROUP_M = 3
 GEMM_OPT_TC_GROUP_M = 4
 GEMM_OPT_MAX_CTAS = 5
 GEMM_OPT_SIMT_CONFIG = 6
+GEMM_OPT_SPLIT_K = 7
 
 DTYPES = {"f32": GEMM_F32, "tf32": GEMM_TF32, "bf16": GEMM_BF16}
 LAYOUTS = {"row": GEMM_B_ROW_MAJOR, "col": GEMM_B_COL_MAJOR}

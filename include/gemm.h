@@ -36,7 +36,8 @@
  * Ownership and threading: the caller owns A, B, C and the stream.  A handle
  * owns a small device status word and a device workspace that grows on
  * demand (used to re-pack operands whose address or leading dimension is not
- * a multiple of 16 bytes, and by gemm_run_host).  Calls on one handle must be
+ * a multiple of 16 bytes, for the K-slice partial products of small FP32
+ * problems, and by gemm_run_host).  Calls on one handle must be
  * issued from one host thread at a time and be ordered on the GPU (one
  * stream, or streams the caller orders), because they share the workspace.
  *
@@ -81,6 +82,7 @@ extern "C" {
 #define GEMM_OPT_TC_GROUP_M 4     /* tile-order group height in tiles for the tensor-core kernel */
 #define GEMM_OPT_MAX_CTAS 5       /* cap on persistent CTAs (0 = SMs x resident CTAs per SM) */
 #define GEMM_OPT_SIMT_CONFIG 6    /* FP32 tile configuration: 0 = chosen per shape, else 1..6 */
+#define GEMM_OPT_SPLIT_K 7        /* FP32 K slices: 0 = chosen per shape, 1 = none, 2..64 = forced */
 
 typedef struct gemm_ctx *gemm_handle_t;
 

@@ -226,6 +226,48 @@ def test_launch_count_increments(g):
     assert g.launch_count == before + 1
 
 
+# ------------------------------------------------------- split-K (FP32 path)
+
+@pytest.mark.parametrize("layout", [ROW, COL])
+@pytest.mark.parametrize("splits", [2, 3, 7])
+def test_split_k_forced(g, oracle_mod, layout, splits):
+    """K cut into slices whose partial products are summed in a second
+    kernel ("GEMM 性能优化", 台阶 1): same tolerance, deterministic."""
+    from dense_gemm_sm100_gb300 import gemm
+    M, N, K = 200, 333, 1000
+    A, B = inp.make_operands(M, N, K, layout_b=layout, dist="normal", seed=61 + splits)
+    g.set_option(gemm.GEMM_OPT_SPLIT_K, splits)
+    try:
+        C1 = run_gpu(g, A, B, layout, "f32").cpu()
+        assert f"splitk{splits}" in g.last_path
+        C2 = run_gpu(g, A, B, layout, "f32").cpu()
+    finally:
+        g.set_option(gemm.GEMM_OPT_SPLIT_K, 0)
+    assert torch.equal(C1, C2)
+    Cr, S = oracle_of(oracle_mod, A, B, layout)
+    assert_parity(C1, Cr, S, TOL["f32"], f"split {splits}")
+
+
+def test_split_k_integer_exact(g, oracle_mod):
+    from dense_gemm_sm100_gb300 import gemm
+    A, B = inp.make_integer_operands(150, 260, 900, seed=71)
+    g.set_option(gemm.GEMM_OPT_SPLIT_K, 4)
+    try:
+        C = run_gpu(g, A, B, ROW, "f32")
+        assert "splitk4" in g.last_path
+    finally:
+        g.set_option(gemm.GEMM_OPT_SPLIT_K, 0)
+    Cr, _ = oracle_of(oracle_mod, A, B, ROW)
+    assert np.array_equal(to_f64(C), Cr)
+
+
+def test_split_k_chosen_for_underfilled_shape(g):
+    """1024^3 fills 64 of the SMs with 128x128 tiles: split-K is chosen."""
+    A, B = inp.make_operands(1024, 1024, 1024, layout_b=COL, seed=1)
+    run_gpu(g, A, B, COL, "f32")
+    assert "splitk" in g.last_path
+
+
 # ------------------------------------------------------- the five workloads
 
 def _sampled_check(g, oracle_mod, w, n_rows=40, n_cols=40):
