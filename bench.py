@@ -45,7 +45,9 @@ NOMINAL_PF = {"bf16": 2.25, "tf32": 1.1}
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture of the kernel as it is now; None until captured for this version.
 # Key: workload name -> (bytes per launch, summary file under profiles/).
-NCU_TRAFFIC: dict[str, tuple[float, str]] = {}
+NCU_TRAFFIC: dict[str, tuple[float, str]] = {
+    "fp32_8192_row": (3309.6e6 + 261.1e6, "profiles/dram_traffic_full_size.md"),
+}
 
 DESCRIPTIONS = {
     "fp32_8192_row": "FP32 SIMT GEMM M=N=K=8192, A/B/C row-major, U[-1,1) seed 3",
@@ -374,10 +376,22 @@ def main(argv=None):
     modes = []
     if not args.no_modes:
         for name in TC_WORKLOADS:
-            r = bench_workload(g, name, max(args.steps, 100), args.warmup, ctx, peaks, peak_note,
+            msampler = ClockSampler(dev_index) if rank0 else None
+            if msampler:
+                msampler.start()
+            r = bench_workload(g, name, max(args.steps, 200), args.warmup, ctx, peaks, peak_note,
                                with_e2e=False)
-            modes.append({k: r[k] for k in ("workload", "description", "dtype", "value",
-                                            "ms_per_step", "kernel_ms", "path", "roofline")})
+            m = {k: r[k] for k in ("workload", "description", "dtype", "value",
+                                   "ms_per_step", "kernel_ms", "path", "roofline")}
+            if msampler:
+                msampler.stop()
+                m["clocks"] = msampler.summary(*r["wall_window"])
+                if m["clocks"] and m["clocks"].get("sm_mhz"):
+                    # the same peak scaled to the SM clock seen while this mode ran
+                    f = m["clocks"]["sm_mhz"] / peaks["sm_max_mhz"]
+                    m["roofline"]["frac_at_observed_clock"] = round(
+                        m["roofline"]["achieved"] / (m["roofline"]["peak"] * f), 4) if f > 0 else None
+            modes.append(m)
     e2e = None
     if not args.no_e2e:
         r = bench_workload(g, args.workload, min(args.steps, 10), args.warmup, ctx, peaks,

@@ -29,6 +29,8 @@ struct gemm_ctx {
     int max_ctas = 0;
     int simt_config = 0;  // 0: chosen per shape; else configuration index + 1
     int split_k = 0;      // 0: chosen per shape; 1: never; n > 1: n K slices (FP32 path)
+    int tc_cluster = 3;   // tensor-core mode: 1 one CTA per tile, 2 multicast pairs, 3 pair MMA
+    int tc_tma_store = 1; // tensor-core epilogue writes C with TMA stores when C allows it
 };
 
 namespace {
@@ -295,16 +297,23 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
             rc = encode_2d(h, &tmB, es, B, N, K, ldb, 128 / es, bk,
                            es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B);
         else
-            rc = encode_2d(h, &tmB, es, B, K, N, ldb, bk, dg::kTcBN);
+            rc = encode_2d(h, &tmB, es, B, K, N, ldb, bk, dg::kTcBoxBCol);
         if (rc) return rc;
-        const int tiles = static_cast<int>(((M + dg::kTcBM - 1) / dg::kTcBM) *
-                                           ((N + dg::kTcBN - 1) / dg::kTcBN));
-        lc.grid = dg::tc_grid(tiles, h->max_ctas > 0 ? h->max_ctas : h->sm_count);
+        const int cluster = h->tc_cluster >= 2 && M > dg::kTcBM ? h->tc_cluster : 1;
+        int grid = dg::tc_grid(M, N, h->max_ctas > 0 ? h->max_ctas : h->sm_count, cluster);
+        lc.grid = grid;
         lc.group_m = h->tc_group_m;
-        cudaError_t e = dg::launch_tc(dtype, layout_b, tmA, tmB, static_cast<int>(M), static_cast<int>(N),
-                                      static_cast<int>(K), C, ldc, c_vec4, lc);
+        alignas(64) CUtensorMap tmC;
+        const bool c_tma = c_vec4 && h->tc_tma_store;
+        if (c_tma) {
+            rc = encode_2d(h, &tmC, 4, C, N, M, ldc, dg::kTcBoxC, dg::kTcBoxC);
+            if (rc) return rc;
+        }
+        cudaError_t e = dg::launch_tc(dtype, layout_b, tmA, tmB, c_tma ? &tmC : nullptr, static_cast<int>(M),
+                                      static_cast<int>(N), static_cast<int>(K), C, ldc, c_vec4, lc, cluster);
         if (e != cudaSuccess) return cuda_fail(h, e, "tensor-core kernel launch");
-        path = std::string(dtype == GEMM_BF16 ? "tc_bf16" : "tc_tf32") + "_128x256_" + lay + path;
+        path = std::string(dtype == GEMM_BF16 ? "tc_bf16" : "tc_tf32") +
+               (cluster == 3 ? "_pair256x256_" : "_128x256_") + lay + (cluster == 2 ? "_cluster2" : "") + path;
     }
     ++h->launches;
     h->last_path = path;
@@ -504,6 +513,14 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value)
     case GEMM_OPT_SIMT_CONFIG:
         if (value < 0 || value > dg::simt_num_configs()) break;
         h->simt_config = static_cast<int>(value);
+        return GEMM_OK;
+    case GEMM_OPT_TC_TMA_STORE:
+        if (value != 0 && value != 1) break;
+        h->tc_tma_store = static_cast<int>(value);
+        return GEMM_OK;
+    case GEMM_OPT_TC_CLUSTER:
+        if (value < 1 || value > 3) break;
+        h->tc_cluster = static_cast<int>(value);
         return GEMM_OK;
     case GEMM_OPT_SPLIT_K:
         if (value < 0 || value > 64) break;

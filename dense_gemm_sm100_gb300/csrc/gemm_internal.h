@@ -35,9 +35,12 @@ SplitK simt_pick_splits(int config, int layout_b, int64_t M, int64_t N, int64_t 
 
 // Geometry of the tensor-core kernel (gemm_tc.cu).  A tile of C is
 // kTcBM x kTcBN; every stage holds 128 bytes of K per operand row, i.e.
-// 64 BF16 or 32 TF32 elements.
+// 64 BF16 or 32 TF32 elements.  TMA boxes (innermost first): A {bk, kTcBM};
+// row-major B {128/es, bk}, kTcBN*es/128 boxes per stage; column-major B
+// {bk, kTcBoxBCol}, two boxes per stage.
 constexpr int kTcBM = 128;
 constexpr int kTcBN = 256;
+constexpr int kTcBoxBCol = 128;
 constexpr int tc_bk(int elem_bytes) { return 128 / elem_bytes; }
 
 struct LaunchCommon {
@@ -62,11 +65,18 @@ cudaError_t launch_simt_f32(int config, const CUtensorMap &tmA, const CUtensorMa
                             int layout_b, int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
                             const LaunchCommon &lc, const SplitK &sk = SplitK());
 
-// Tensor-core GEMM; dtype is GEMM_TF32 or GEMM_BF16.  tmA/tmB as above with
-// 128-byte rows (BK elements) and the tensor-core boxes.
+// Tensor-core GEMM; dtype is GEMM_TF32 or GEMM_BF16.  tmA/tmB as above.
+// tmC (may be null): C as FP32 dims {N, M}, box {32, 32}, 128-byte swizzle,
+// used for TMA stores; null means per-thread stores.  cluster = 2 runs CTA
+// pairs that share (multicast) the B tile; cluster = 3 runs the pair MMA
+// (cta_group::2, 256x256 per pair); lc.grid must then be even.
+constexpr int kTcBoxC = 32;
 cudaError_t launch_tc(int dtype, int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                      int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
-                      const LaunchCommon &lc);
+                      const CUtensorMap *tmC, int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
+                      const LaunchCommon &lc, int cluster);
+
+// Persistent grid of the tensor-core kernel: one CTA per SM, whole clusters.
+int tc_grid(int64_t M, int64_t N, int sm_count, int cluster);
 
 // dst[r*ldd + c] = src[r*lds + c] for r < rows, c < cols (elem_bytes 2 or 4).
 cudaError_t launch_repack(const void *src, int64_t lds, void *dst, int64_t ldd, int64_t rows,
@@ -81,7 +91,5 @@ cudaError_t launch_splitk_reduce(const float *partials, int splits, float *C, in
 cudaError_t launch_zero_fill(float *C, int64_t ldc, int64_t M, int64_t N, int sm_count,
                              cudaStream_t stream);
 
-// Persistent-grid size the tensor-core kernel wants for `tiles` output tiles.
-int tc_grid(int tiles, int sm_count);
 
 }  // namespace dg

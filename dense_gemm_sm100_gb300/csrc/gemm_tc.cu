@@ -10,17 +10,26 @@
 //    from one thread, issues tcgen05.mma (M=128, N=256, K=32 bytes per
 //    instruction); tcgen05.commit releases ring stages and announces a
 //    finished accumulator;
-//  * warps 2-5: epilogue, tcgen05.ld of their 32 TMEM lanes, guarded stores
-//    of C.  With two accumulators the epilogue of one tile overlaps the
-//    main loop of the next.
-//  * persistent grid (one CTA per SM) walking tiles in groups of `group_m`
-//    tile rows for L2 reuse ("GEMM 性能优化", Wave 模型与 L2 命中率).
+//  * warps 2-5: epilogue, tcgen05.ld of their 32 TMEM lanes; each 32x32 FP32
+//    chunk is staged in 128-byte-swizzled shared memory and written by one
+//    TMA store (whole 128-byte lines; TMA clips the M and N edges).  With two
+//    accumulators the epilogue of one tile overlaps the main loop of the
+//    next.  A C that TMA cannot address (pitch or base not 16-byte aligned)
+//    takes guarded per-thread stores instead.
+//  * persistent grid walking tiles in groups of `group_m` tile rows for L2
+//    reuse ("GEMM 性能优化", Wave 模型与 L2 命中率).
+//  * CL = 2: CTAs run in clusters of two that own vertically adjacent tiles
+//    (same B columns).  Each CTA loads its own A and one half of the shared B
+//    tile, multicast into both CTAs' shared memory, so every SM reads 32 KB
+//    instead of 48 KB from L2 per stage (data reuse one level further out
+//    than the pages' shared-memory tiling).  Each MMA's commit releases the
+//    ring slot in both CTAs.
 // A is K-major.  B is K-major when stored column-major (the corner-turning
 // case of "PMPP Chapter 06: Performance considerations", section 1) and
 // MN-major when stored row-major; the shared-memory descriptor says which,
 // so no transpose pass is needed.  MN-major TF32 tiles are staged with the
-// 32-byte-atom variant of the 128-byte swizzle.  Out-of-range elements are zero-filled by
-// TMA and stores are guarded, so any M, N, K works.
+// 32-byte-atom variant of the 128-byte swizzle.  Out-of-range elements are
+// zero-filled by TMA and stores are guarded, so any M, N, K works.
 #include <cstdint>
 
 #include "../../include/gemm.h"
@@ -38,9 +47,14 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 512;  // two accumulators of BN columns
 constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+// Epilogue staging: per epilogue warp two 32x32 FP32 chunks (4 KB each,
+// 128-byte swizzled) that TMA stores to C.
+constexpr int EPI_CHUNK_BYTES = 32 * 32 * 4;
+constexpr int EPI_BYTES = 4 * 2 * EPI_CHUNK_BYTES;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8 + 16;
 static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 static_assert(SMEM_BYTES > 116 * 1024, "one CTA per SM: TMEM allocation assumes it");
+static_assert(kTcBoxBCol == BN / 2, "column-major B is loaded in two halves");
 
 struct TcParams {
     int M, N, K;
@@ -50,16 +64,23 @@ struct TcParams {
     int *status;
     unsigned long long timeout_ns;
     int c_vec4;
+    int c_tma;  // 1: C is written by TMA stores through tmC
 };
 
-__device__ __forceinline__ void tile_coords(int t, const TcParams &p, int &mb, int &nb)
+// Unit u of the grouped order over (tile-row groups of CL tiles) x tiles_n:
+// groups of `group_m` units along M, column-major inside a group, so CTAs
+// running at the same time share A and B panels.  The CTA of cluster rank r
+// takes tile row CL*um + r.
+template <int CL>
+__device__ __forceinline__ void unit_coords(int u, const TcParams &p, uint32_t rank, int &mb, int &nb)
 {
+    const int units_m = (p.tiles_m + CL - 1) / CL;
     const int per_group = p.group_m * p.tiles_n;
-    const int g = t / per_group;
+    const int g = u / per_group;
     const int first_m = g * p.group_m;
-    const int gm = min(p.tiles_m - first_m, p.group_m);
-    const int r = t - g * per_group;
-    mb = first_m + r % gm;
+    const int gm = min(units_m - first_m, p.group_m);
+    const int r = u - g * per_group;
+    mb = CL * (first_m + r % gm) + static_cast<int>(rank);
     nb = r / gm;
 }
 
@@ -71,19 +92,21 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t fmt, uint32_t b_mn_ma
            (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
 }
 
-// DT: 0 = BF16 (2-byte elements), 1 = TF32 (4-byte elements).
-template <int DT, int LAYOUT_B>
+// DT: 0 = BF16 (2-byte elements), 1 = TF32 (4-byte elements).  CL: CTAs per
+// cluster sharing the B tile (1 or 2).
+template <int DT, int LAYOUT_B, int CL>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmB, const TcParams p)
+                   const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const TcParams p)
 {
     constexpr int ES = DT == 0 ? 2 : 4;
-    constexpr int BK = 128 / ES;        // K elements per stage
-    constexpr int UMMA_K = 32 / ES;     // K elements per MMA instruction
+    constexpr int BK = 128 / ES;          // K elements per stage
+    constexpr int UMMA_K = 32 / ES;       // K elements per MMA instruction
     constexpr int K_STEPS = BK / UMMA_K;  // 4
-    constexpr int BOX_N = 128 / ES;     // row-major B: N elements per TMA box
+    constexpr int BOX_N = 128 / ES;       // row-major B: N elements per TMA box
     constexpr int B_BOXES = BN / BOX_N;
-    constexpr int BOX_BYTES = BK * 128;  // one row-major B box
+    constexpr int BOX_BYTES = BK * 128;   // one row-major B box
     constexpr uint32_t IDESC = make_idesc(DT == 0 ? 1u : 2u, LAYOUT_B == 0 ? 1u : 0u);
     // An MN-major operand of 32-bit elements uses the 128-byte swizzle with
     // 32-byte atoms (the row-major B tensor map is encoded to match); its
@@ -91,31 +114,36 @@ __global__ void __launch_bounds__(THREADS, 1)
     // the descriptor is 4 x 128 bytes instead of 8 x 128 bytes.
     constexpr uint32_t B_MN_LAYOUT = DT == 0 ? kLayoutSw128 : kLayoutSw128Atom32;
     constexpr uint32_t B_MN_SBO = DT == 0 ? 1024u : 512u;
+    constexpr uint16_t CLUSTER_MASK = (1u << CL) - 1u;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t pad = ((raw_addr + 1023u) & ~1023u) - raw_addr;
     uint8_t *smem = smem_raw + pad;
     const uint32_t sbase = raw_addr + pad;
-    const uint32_t bars = sbase + STAGES * STAGE_BYTES;
+    const uint32_t epi_base = sbase + STAGES * STAGE_BYTES;  // EPI_BYTES, 1024-aligned
+    const uint32_t bars = epi_base + EPI_BYTES;
     const uint32_t full_bar = bars;                      // [STAGES]
     const uint32_t empty_bar = bars + 8 * STAGES;        // [STAGES]
     const uint32_t tfull_bar = bars + 16 * STAGES;       // [2]
     const uint32_t tempty_bar = tfull_bar + 16;          // [2]
     const uint32_t drain_bar = tempty_bar + 16;          // [1]
-    uint8_t *tail = smem + STAGES * STAGE_BYTES + NUM_BARS * 8;
+    uint8_t *tail = smem + STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8;
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(tail);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tail + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int num_tiles = p.tiles_m * p.tiles_n;
+    const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
+    const int cluster = blockIdx.x / CL;
+    const int clusters = gridDim.x / CL;
+    const int num_units = ((p.tiles_m + CL - 1) / CL) * p.tiles_n;
     const int k_tiles = (p.K + BK - 1) / BK;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar + 8 * s, 1);
-            mbar_init(empty_bar + 8 * s, 1);
+            mbar_init(empty_bar + 8 * s, CL);  // one release per MMA issuer of the cluster
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar + 8 * b, 1);
@@ -130,7 +158,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_relinquish();
     }
     tc_fence_before_sync();
-    __syncthreads();
+    if (CL > 1)
+        cluster_sync();  // peers' barriers are initialised before anyone targets them
+    else
+        __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -141,9 +172,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_prefetch_desc(&tmB);
             uint32_t it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int u = cluster; ok && u < num_units; u += clusters) {
                 int mb, nb;
-                tile_coords(tile, p, mb, nb);
+                unit_coords<CL>(u, p, rank, mb, nb);
                 for (int kt = 0; kt < k_tiles; ++kt, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
@@ -155,24 +186,49 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t fb = full_bar + 8 * s;
                     const uint32_t a_st = sbase + s * STAGE_BYTES;
                     const uint32_t b_st = a_st + A_BYTES;
+                    // A of this CTA, plus all of B: this CTA's half and (CL = 2)
+                    // the peer's half, which the peer multicasts here.
                     mbar_arrive_expect_tx(fb, STAGE_BYTES);
                     tma_load_2d(a_st, &tmA, fb, kt * BK, mb * BM);
                     if (LAYOUT_B == 0) {
+                        if (CL == 1) {
 #pragma unroll
-                        for (int j = 0; j < B_BOXES; ++j)
-                            tma_load_2d(b_st + j * BOX_BYTES, &tmB, fb, nb * BN + j * BOX_N, kt * BK);
+                            for (int j = 0; j < B_BOXES; ++j)
+                                tma_load_2d(b_st + j * BOX_BYTES, &tmB, fb, nb * BN + j * BOX_N, kt * BK);
+                        } else {
+#pragma unroll
+                            for (int jj = 0; jj < B_BOXES / 2; ++jj) {
+                                const int j = static_cast<int>(rank) * (B_BOXES / 2) + jj;
+                                tma_load_2d_multicast(b_st + j * BOX_BYTES, &tmB, fb, nb * BN + j * BOX_N,
+                                                      kt * BK, CLUSTER_MASK);
+                            }
+                        }
                     } else {
-                        tma_load_2d(b_st, &tmB, fb, kt * BK, nb * BN);
+                        if (CL == 1) {
+                            tma_load_2d(b_st, &tmB, fb, kt * BK, nb * BN);
+                            tma_load_2d(b_st + B_BYTES / 2, &tmB, fb, kt * BK, nb * BN + BN / 2);
+                        } else {
+                            tma_load_2d_multicast(b_st + rank * (B_BYTES / 2), &tmB, fb, kt * BK,
+                                                  nb * BN + static_cast<int>(rank) * (BN / 2), CLUSTER_MASK);
+                        }
                     }
                 }
             }
             if (!ok) {
+                // Leave no copy in flight: wait (bounded) for the stages issued last.
                 const uint32_t n = it < (uint32_t)STAGES ? it : (uint32_t)STAGES;
                 for (uint32_t i = it - n; i < it; ++i) {
                     int dummy = 0;
                     mbar_wait(full_bar + 8 * (i % STAGES), (i / STAGES) & 1u, &dummy, nullptr,
                               kWaitDrain, p.timeout_ns);
                 }
+            } else if (CL > 1) {
+                // Every release of the last stages (this CTA's MMA and the
+                // peer's) must have landed before shared memory goes away.
+                const uint32_t n = it < (uint32_t)STAGES ? it : (uint32_t)STAGES;
+                for (uint32_t i = it - n; i < it; ++i)
+                    mbar_wait(empty_bar + 8 * (i % STAGES), (i / STAGES) & 1u, abort_flag, p.status,
+                              kWaitDrain, p.timeout_ns);
             }
         }
     } else if (warp == 1) {
@@ -180,7 +236,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             uint32_t it = 0, acc_it = 0;
             bool ok = true, issued = false;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++acc_it) {
+            for (int u = cluster; ok && u < num_units; u += clusters, ++acc_it) {
                 const uint32_t abuf = acc_it & 1u;
                 const uint32_t aph = (acc_it >> 1) & 1u;
                 if (!mbar_wait(tempty_bar + 8 * abuf, aph ^ 1u, abort_flag, p.status,
@@ -215,7 +271,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                             tc_mma_tf32(d_tmem, adesc, bdesc, IDESC, accumulate);
                     }
                     issued = true;
-                    tc_commit(empty_bar + 8 * s);
+                    if (CL == 1)
+                        tc_commit(empty_bar + 8 * s);
+                    else
+                        tc_commit_multicast(empty_bar + 8 * s, CLUSTER_MASK);
                 }
                 if (!ok) break;
                 tc_commit(tfull_bar + 8 * abuf);
@@ -231,10 +290,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;
+        const uint32_t stage_buf = epi_base + static_cast<uint32_t>((warp - 2) * 2 * EPI_CHUNK_BYTES);
+        if (p.c_tma && lane == 0) tma_prefetch_desc(&tmC);
         uint32_t acc_it = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++acc_it) {
+        for (int u = cluster; u < num_units; u += clusters, ++acc_it) {
             int mb, nb;
-            tile_coords(tile, p, mb, nb);
+            unit_coords<CL>(u, p, rank, mb, nb);
             const uint32_t abuf = acc_it & 1u;
             const uint32_t aph = (acc_it >> 1) & 1u;
             bool ok = true;
@@ -252,8 +313,34 @@ __global__ void __launch_bounds__(THREADS, 1)
                 uint32_t v[32];
                 tmem_load_32cols(t_row + c * 32, v);
                 tmem_wait_ld();
-                if (m < p.M) {
-                    const int n0 = nb * BN + c * 32;
+                if (c == BN / 32 - 1) {
+                    // The accumulator is in registers: hand TMEM back to the MMA warp.
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty_bar + 8 * abuf);
+                }
+                const int n0 = nb * BN + c * 32;
+                if (p.c_tma) {
+                    // Row `lane` of a 32x32 chunk, 128-byte swizzled (chunk j
+                    // of row r at 16*(j ^ (r & 7))), then one TMA store of the
+                    // chunk; TMA drops the rows and columns outside C.
+                    const uint32_t buf = stage_buf + static_cast<uint32_t>(c & 1) * EPI_CHUNK_BYTES;
+                    if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t addr = buf + lane * 128 + ((j ^ (lane & 7)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[4 * j]),
+                                     "r"(v[4 * j + 1]), "r"(v[4 * j + 2]), "r"(v[4 * j + 3])
+                                     : "memory");
+                    }
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, buf, n0, mb * BM + q * 32);
+                        bulk_commit_group();
+                    }
+                } else if (m < p.M) {
                     if (p.c_vec4 && n0 + 31 < p.N) {
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
@@ -267,43 +354,364 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
             }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar + 8 * abuf);
         }
+        if (p.c_tma && lane == 0) bulk_wait_group_all();  // stores done before shared memory goes away
+        __syncwarp();
     }
 
     tc_fence_before_sync();
-    __syncthreads();
+    __syncwarp();
+    if (CL > 1)
+        cluster_sync();  // no CTA leaves while its peer may still target its shared memory
+    else
+        __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
+// ---------------------------------------------------------------------------
+// Pair kernel: one 256 x 256 tile per cluster of two CTAs, computed by
+// tcgen05.mma.cta_group::2 issued from the even CTA.  Each CTA stages only
+// its 128 rows of A and its 128 columns of B (32 KB per stage instead of
+// 48 KB), so six stages fit where the one-CTA kernel holds four: more bytes
+// in flight per unit of MMA work.  D rows of CTA r live in CTA r's TMEM.
+constexpr int P_STAGES = 6;
+constexpr int P_A_BYTES = BM * 128;        // 16 KiB
+constexpr int P_B_BYTES = (BN / 2) * 128;  // 16 KiB: this CTA's half of B
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+constexpr int P_NUM_BARS = 2 * P_STAGES + 2 + 2 + 1;
+constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + EPI_BYTES + P_NUM_BARS * 8 + 16;
+static_assert(P_STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+static_assert(P_SMEM_BYTES > 116 * 1024 && P_SMEM_BYTES <= 227 * 1024, "one CTA per SM");
+
+template <int DT, int LAYOUT_B>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const TcParams p)
+{
+    constexpr int ES = DT == 0 ? 2 : 4;
+    constexpr int BK = 128 / ES;
+    constexpr int UMMA_K = 32 / ES;
+    constexpr int K_STEPS = BK / UMMA_K;
+    constexpr int BOX_N = 128 / ES;              // row-major B: N elements per TMA box
+    constexpr int B_HALF_BOXES = (BN / 2) / BOX_N;
+    constexpr int BOX_BYTES = BK * 128;
+    // M = 256 across the pair, N = 256.
+    constexpr uint32_t IDESC = (1u << 4) | ((DT == 0 ? 1u : 2u) << 7) | ((DT == 0 ? 1u : 2u) << 10) |
+                               ((LAYOUT_B == 0 ? 1u : 0u) << 16) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                               (static_cast<uint32_t>((2 * BM) >> 4) << 24);
+    constexpr uint32_t B_MN_LAYOUT = DT == 0 ? kLayoutSw128 : kLayoutSw128Atom32;
+    constexpr uint32_t B_MN_SBO = DT == 0 ? 1024u : 512u;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t pad = ((raw_addr + 1023u) & ~1023u) - raw_addr;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t sbase = raw_addr + pad;
+    const uint32_t epi_base = sbase + P_STAGES * P_STAGE_BYTES;
+    const uint32_t bars = epi_base + EPI_BYTES;
+    const uint32_t full_bar = bars;                    // [P_STAGES], used in the even CTA
+    const uint32_t empty_bar = bars + 8 * P_STAGES;    // [P_STAGES], both CTAs
+    const uint32_t tfull_bar = bars + 16 * P_STAGES;   // [2], both CTAs
+    const uint32_t tempty_bar = tfull_bar + 16;        // [2], used in the even CTA
+    const uint32_t drain_bar = tempty_bar + 16;        // [1]
+    uint8_t *tail = smem + P_STAGES * P_STAGE_BYTES + EPI_BYTES + P_NUM_BARS * 8;
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(tail);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tail + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int cluster = blockIdx.x / 2;
+    const int clusters = gridDim.x / 2;
+    const int num_units = ((p.tiles_m + 1) / 2) * p.tiles_n;
+    const int k_tiles = (p.K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P_STAGES; ++s) {
+            mbar_init(full_bar + 8 * s, 1);   // the even CTA's producer; bytes from both CTAs
+            mbar_init(empty_bar + 8 * s, 1);  // the pair commit
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar + 8 * b, 1);   // the pair commit
+            mbar_init(tempty_bar + 8 * b, 8);  // 4 epilogue warps in each CTA
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_addr(const_cast<uint32_t *>(tmem_slot)), TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before_sync();
+    cluster_sync();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int u = cluster; ok && u < num_units; u += clusters) {
+                int mb, nb;
+                unit_coords<2>(u, p, rank, mb, nb);
+                for (int kt = 0; kt < k_tiles; ++kt, ++it) {
+                    const uint32_t s = it % P_STAGES;
+                    const uint32_t ph = (it / P_STAGES) & 1u;
+                    if (!mbar_wait(empty_bar + 8 * s, ph ^ 1u, abort_flag, p.status,
+                                   kWaitProducerEmpty, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb_local = full_bar + 8 * s;
+                    const uint32_t fb = mapa_shared(fb_local, 0);  // the even CTA's barrier
+                    const uint32_t a_st = sbase + s * P_STAGE_BYTES;
+                    const uint32_t b_st = a_st + P_A_BYTES;
+                    if (leader) mbar_arrive_expect_tx(fb_local, 2 * P_STAGE_BYTES);
+                    tma_load_2d_pair(a_st, &tmA, fb, kt * BK, mb * BM);
+                    const int n_half = nb * BN + static_cast<int>(rank) * (BN / 2);
+                    if (LAYOUT_B == 0) {
+#pragma unroll
+                        for (int j = 0; j < B_HALF_BOXES; ++j)
+                            tma_load_2d_pair(b_st + j * BOX_BYTES, &tmB, fb, n_half + j * BOX_N, kt * BK);
+                    } else {
+                        tma_load_2d_pair(b_st, &tmB, fb, kt * BK, n_half);
+                    }
+                }
+            }
+            // Every release of the last stages must have landed here before
+            // shared memory goes away (and, after an abort, every copy).
+            const uint32_t n = it < (uint32_t)P_STAGES ? it : (uint32_t)P_STAGES;
+            for (uint32_t i = it - n; i < it; ++i) {
+                int dummy = 0;
+                mbar_wait(empty_bar + 8 * (i % P_STAGES), (i / P_STAGES) & 1u, ok ? abort_flag : &dummy,
+                          ok ? p.status : nullptr, kWaitDrain, p.timeout_ns);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer (even CTA)
+        if (leader && lane == 0) {
+            uint32_t it = 0, acc_it = 0;
+            bool ok = true, issued = false;
+            for (int u = cluster; ok && u < num_units; u += clusters, ++acc_it) {
+                const uint32_t abuf = acc_it & 1u;
+                const uint32_t aph = (acc_it >> 1) & 1u;
+                if (!mbar_wait(tempty_bar + 8 * abuf, aph ^ 1u, abort_flag, p.status,
+                               kWaitMmaTmemEmpty, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + abuf * BN;
+                for (int kt = 0; kt < k_tiles; ++kt, ++it) {
+                    const uint32_t s = it % P_STAGES;
+                    const uint32_t ph = (it / P_STAGES) & 1u;
+                    if (!mbar_wait(full_bar + 8 * s, ph, abort_flag, p.status, kWaitMmaFull,
+                                   p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a_st = sbase + s * P_STAGE_BYTES;
+                    const uint32_t b_st = a_st + P_A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < K_STEPS; ++kk) {
+                        const uint64_t adesc = smem_desc(a_st + kk * 32, 16, 1024, kLayoutSw128);
+                        const uint64_t bdesc =
+                            LAYOUT_B == 0
+                                ? smem_desc(b_st + kk * UMMA_K * 128, BOX_BYTES, B_MN_SBO, B_MN_LAYOUT)
+                                : smem_desc(b_st + kk * 32, 16, 1024, kLayoutSw128);
+                        const uint32_t accumulate = (kt > 0 || kk > 0) ? 1u : 0u;
+                        if (DT == 0)
+                            tc_mma_f16_pair(d_tmem, adesc, bdesc, IDESC, accumulate);
+                        else
+                            tc_mma_tf32_pair(d_tmem, adesc, bdesc, IDESC, accumulate);
+                    }
+                    issued = true;
+                    tc_commit_pair_multicast(empty_bar + 8 * s, 0x3);
+                }
+                if (!ok) break;
+                tc_commit_pair_multicast(tfull_bar + 8 * abuf, 0x3);
+            }
+            if (!ok && issued) {
+                tc_commit_pair_multicast(drain_bar, 0x1);
+                int dummy = 0;
+                mbar_wait(drain_bar, 0, &dummy, nullptr, kWaitDrain, p.timeout_ns);
+            }
+        }
+    } else {
+        // ------------------------------------------------------ epilogue (both CTAs)
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const uint32_t stage_buf = epi_base + static_cast<uint32_t>((warp - 2) * 2 * EPI_CHUNK_BYTES);
+        if (p.c_tma && lane == 0) tma_prefetch_desc(&tmC);
+        uint32_t acc_it = 0;
+        for (int u = cluster; u < num_units; u += clusters, ++acc_it) {
+            int mb, nb;
+            unit_coords<2>(u, p, rank, mb, nb);
+            const uint32_t abuf = acc_it & 1u;
+            const uint32_t aph = (acc_it >> 1) & 1u;
+            bool ok = true;
+            if (lane == 0)
+                ok = mbar_wait(tfull_bar + 8 * abuf, aph, abort_flag, p.status, kWaitEpiTmemFull,
+                               p.timeout_ns);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
+            tc_fence_after_sync();
+            const long long m = (long long)mb * BM + row;
+            float *crow = p.C + m * p.ldc;
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + abuf * BN;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t v[32];
+                tmem_load_32cols(t_row + c * 32, v);
+                tmem_wait_ld();
+                if (c == BN / 32 - 1) {
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (leader)
+                            mbar_arrive(tempty_bar + 8 * abuf);
+                        else
+                            mbar_arrive_cluster(mapa_shared(tempty_bar + 8 * abuf, 0));
+                    }
+                }
+                const int n0 = nb * BN + c * 32;
+                if (p.c_tma) {
+                    const uint32_t buf = stage_buf + static_cast<uint32_t>(c & 1) * EPI_CHUNK_BYTES;
+                    if (lane == 0) bulk_wait_group_read<1>();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t addr = buf + lane * 128 + ((j ^ (lane & 7)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[4 * j]),
+                                     "r"(v[4 * j + 1]), "r"(v[4 * j + 2]), "r"(v[4 * j + 3])
+                                     : "memory");
+                    }
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, buf, n0, mb * BM + q * 32);
+                        bulk_commit_group();
+                    }
+                } else if (m < p.M) {
+                    if (p.c_vec4 && n0 + 31 < p.N) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            *reinterpret_cast<float4 *>(crow + n0 + 4 * j) =
+                                make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                            __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (n0 + j < p.N) crow[n0 + j] = __uint_as_float(v[j]);
+                    }
+                }
+            }
+        }
+        if (p.c_tma && lane == 0) bulk_wait_group_all();
+        __syncwarp();
+    }
+
+    tc_fence_before_sync();
+    __syncwarp();
+    cluster_sync();  // no CTA leaves while its peer may still target its shared memory
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
 template <int DT, int L>
+cudaError_t set_pair_attrs()
+{
+    return cudaFuncSetAttribute(gemm_tc_pair_kernel<DT, L>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                P_SMEM_BYTES);
+}
+
+template <int DT, int L>
+cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                        const TcParams &p, int grid, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = P_SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<DT, L>, tmA, tmB, tmC, p);
+}
+
+template <int DT, int L, int CL>
 cudaError_t set_attrs()
 {
-    return cudaFuncSetAttribute(gemm_tc_kernel<DT, L>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(gemm_tc_kernel<DT, L, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 SMEM_BYTES);
+}
+
+template <int DT, int L, int CL>
+cudaError_t launch_one(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                       const TcParams &p, int grid, cudaStream_t stream)
+{
+    if (CL == 1) {
+        gemm_tc_kernel<DT, L, 1><<<grid, THREADS, SMEM_BYTES, stream>>>(tmA, tmB, tmC, p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<DT, L, CL>, tmA, tmB, tmC, p);
 }
 
 }  // namespace
 
 cudaError_t prepare_tc()
 {
-    cudaError_t e = set_attrs<0, 0>();
-    if (e == cudaSuccess) e = set_attrs<0, 1>();
-    if (e == cudaSuccess) e = set_attrs<1, 0>();
-    if (e == cudaSuccess) e = set_attrs<1, 1>();
+    cudaError_t e = cudaSuccess;
+    cudaError_t (*fns[])() = {set_attrs<0, 0, 1>, set_attrs<0, 1, 1>, set_attrs<1, 0, 1>, set_attrs<1, 1, 1>,
+                              set_attrs<0, 0, 2>, set_attrs<0, 1, 2>, set_attrs<1, 0, 2>, set_attrs<1, 1, 2>,
+                              set_pair_attrs<0, 0>, set_pair_attrs<0, 1>, set_pair_attrs<1, 0>,
+                              set_pair_attrs<1, 1>};
+    for (auto f : fns)
+        if (e == cudaSuccess) e = f();
     return e;
 }
 
-int tc_grid(int tiles, int sm_count) { return tiles < sm_count ? tiles : sm_count; }
+int tc_grid(int64_t M, int64_t N, int sm_count, int cluster)
+{
+    const int64_t tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
+    const int cl = cluster >= 2 ? 2 : 1;
+    const int64_t units = ((tiles_m + cl - 1) / cl) * tiles_n;
+    const int64_t clusters = sm_count / cl;
+    return static_cast<int>(cl * (units < clusters ? units : clusters));
+}
 
 cudaError_t launch_tc(int dtype, int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                      int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
-                      const LaunchCommon &lc)
+                      const CUtensorMap *tmC, int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
+                      const LaunchCommon &lc, int cluster)
 {
     TcParams p;
     p.M = M;
@@ -311,25 +719,33 @@ cudaError_t launch_tc(int dtype, int layout_b, const CUtensorMap &tmA, const CUt
     p.K = K;
     p.tiles_m = (M + BM - 1) / BM;
     p.tiles_n = (N + BN - 1) / BN;
-    p.group_m = lc.group_m > 0 ? lc.group_m : 16;
+    const int cl = cluster == 2 ? 2 : cluster == 3 ? 3 : 1;
+    // group_m counts units (tile rows, or tile-row pairs for clusters) along M
+    p.group_m = lc.group_m > 0 ? lc.group_m : (cl >= 2 ? 8 : 16);
     p.C = C;
     p.ldc = ldc;
     p.status = lc.status;
     p.timeout_ns = lc.timeout_ns;
     p.c_vec4 = c_vec4 ? 1 : 0;
-    const dim3 grid(lc.grid), block(THREADS);
-    if (dtype == GEMM_BF16) {
-        if (layout_b == 0)
-            gemm_tc_kernel<0, 0><<<grid, block, SMEM_BYTES, lc.stream>>>(tmA, tmB, p);
-        else
-            gemm_tc_kernel<0, 1><<<grid, block, SMEM_BYTES, lc.stream>>>(tmA, tmB, p);
-    } else {
-        if (layout_b == 0)
-            gemm_tc_kernel<1, 0><<<grid, block, SMEM_BYTES, lc.stream>>>(tmA, tmB, p);
-        else
-            gemm_tc_kernel<1, 1><<<grid, block, SMEM_BYTES, lc.stream>>>(tmA, tmB, p);
+    p.c_tma = tmC != nullptr ? 1 : 0;
+    const CUtensorMap &tc = tmC != nullptr ? *tmC : tmA;  // unused when c_tma == 0
+    const bool bf16 = dtype == GEMM_BF16;
+    if (cl == 3) {
+        if (bf16) return layout_b == 0 ? launch_pair<0, 0>(tmA, tmB, tc, p, lc.grid, lc.stream)
+                                       : launch_pair<0, 1>(tmA, tmB, tc, p, lc.grid, lc.stream);
+        return layout_b == 0 ? launch_pair<1, 0>(tmA, tmB, tc, p, lc.grid, lc.stream)
+                             : launch_pair<1, 1>(tmA, tmB, tc, p, lc.grid, lc.stream);
     }
-    return cudaGetLastError();
+    if (cl == 1) {
+        if (bf16) return layout_b == 0 ? launch_one<0, 0, 1>(tmA, tmB, tc, p, lc.grid, lc.stream)
+                                       : launch_one<0, 1, 1>(tmA, tmB, tc, p, lc.grid, lc.stream);
+        return layout_b == 0 ? launch_one<1, 0, 1>(tmA, tmB, tc, p, lc.grid, lc.stream)
+                             : launch_one<1, 1, 1>(tmA, tmB, tc, p, lc.grid, lc.stream);
+    }
+    if (bf16) return layout_b == 0 ? launch_one<0, 0, 2>(tmA, tmB, tc, p, lc.grid, lc.stream)
+                                   : launch_one<0, 1, 2>(tmA, tmB, tc, p, lc.grid, lc.stream);
+    return layout_b == 0 ? launch_one<1, 0, 2>(tmA, tmB, tc, p, lc.grid, lc.stream)
+                         : launch_one<1, 1, 2>(tmA, tmB, tc, p, lc.grid, lc.stream);
 }
 
 }  // namespace dg

@@ -174,13 +174,11 @@ extern "C" int gemm_run_noalloc(int layout_b, int64_t M, int64_t N, int64_t K, c
         ok = ok && (layout_b == GEMM_B_ROW_MAJOR
                         ? encode(&tmB, es, B, N, K, ldb_p, 128 / es, bk,
                                  es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B)
-                        : encode(&tmB, es, B, K, N, ldb_p, bk, dg::kTcBN, CU_TENSOR_MAP_SWIZZLE_128B));
+                        : encode(&tmB, es, B, K, N, ldb_p, bk, dg::kTcBoxBCol, CU_TENSOR_MAP_SWIZZLE_128B));
         if (!ok) return GEMM_ERR_CUDA;
-        const int tiles = static_cast<int>(((M + dg::kTcBM - 1) / dg::kTcBM) *
-                                           ((N + dg::kTcBN - 1) / dg::kTcBN));
-        lc.grid = dg::tc_grid(tiles, s->sm_count);
-        e = dg::launch_tc(dtype, layout_b, tmA, tmB, static_cast<int>(M), static_cast<int>(N),
-                          static_cast<int>(K), C, ldc, c_vec4, lc);
+        lc.grid = dg::tc_grid(M, N, s->sm_count, 1);
+        e = dg::launch_tc(dtype, layout_b, tmA, tmB, nullptr, static_cast<int>(M), static_cast<int>(N),
+                          static_cast<int>(K), C, ldc, c_vec4, lc, 1);
     }
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

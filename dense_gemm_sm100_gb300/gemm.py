@@ -39,6 +39,8 @@ GEMM_OPT_TC_GROUP_M = 4
 GEMM_OPT_MAX_CTAS = 5
 GEMM_OPT_SIMT_CONFIG = 6
 GEMM_OPT_SPLIT_K = 7
+GEMM_OPT_TC_CLUSTER = 8
+GEMM_OPT_TC_TMA_STORE = 9
 
 DTYPES = {"f32": GEMM_F32, "tf32": GEMM_TF32, "bf16": GEMM_BF16}
 LAYOUTS = {"row": GEMM_B_ROW_MAJOR, "col": GEMM_B_COL_MAJOR}

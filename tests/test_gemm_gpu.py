@@ -176,6 +176,28 @@ def test_layout_invariance(g, mode):
         assert torch.allclose(C1, C2, rtol=0, atol=1e-5 * float(C1.abs().max()) + 1e-30)
 
 
+@pytest.mark.parametrize("mode", ["tf32", "bf16"])
+@pytest.mark.parametrize("shape", [(300, 520, 260), (257, 600, 64)])
+def test_tma_store_epilogue_matches_thread_stores(g, mode, shape):
+    """C written through TMA stores (the default when C is 16-byte aligned)
+    equals C written by per-thread stores, bit for bit, and leaves the ldc
+    padding alone."""
+    from dense_gemm_sm100_gb300 import gemm
+    M, N, K = shape
+    A, B = inp.make_operands(M, N, K, dist="normal", seed=K + 5, dtype=mode)
+    dev = torch.device("cuda", 0)
+    big = torch.full((M, N + 12), float("nan"), device=dev)  # ldc = N + 12 keeps 16-byte rows
+    C_tma = big[:, :N]
+    run_gpu(g, A, B, ROW, mode, C=C_tma)
+    g.set_option(gemm.GEMM_OPT_TC_TMA_STORE, 0)
+    try:
+        C_thr = run_gpu(g, A, B, ROW, mode).cpu()
+    finally:
+        g.set_option(gemm.GEMM_OPT_TC_TMA_STORE, 1)
+    assert torch.equal(C_tma.cpu(), C_thr)
+    assert torch.isnan(big[:, N:].cpu()).all()
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_k_zero_writes_zeros(g, mode):
     dev = torch.device("cuda", 0)
@@ -224,6 +246,38 @@ def test_launch_count_increments(g):
     A, B = inp.make_operands(64, 64, 64, seed=1)
     run_gpu(g, A, B, ROW, "f32")
     assert g.launch_count == before + 1
+
+
+# ------------------------------------------------------- clustered tensor-core kernel
+
+CLUSTER_SHAPES = [(129, 257, 33), (257, 600, 64), (300, 520, 260), (385, 300, 100),
+                  (1000, 40, 300), (640, 1024, 512)]
+
+
+@pytest.mark.parametrize("cluster_mode", [2, 3])
+@pytest.mark.parametrize("mode", ["tf32", "bf16"])
+@pytest.mark.parametrize("layout", [ROW, COL])
+@pytest.mark.parametrize("shape", CLUSTER_SHAPES)
+def test_cluster_pairs_match_oracle_and_single_cta(g, oracle_mod, cluster_mode, mode, layout, shape):
+    """CTA pairs: mode 2 shares the B tile by TMA multicast, mode 3 runs the
+    pair MMA (tcgen05 cta_group::2, 256x256 per pair).  Odd tile-row counts
+    leave one CTA of the last pair entirely out of range.  Same parity, and
+    the same bits as the one-CTA kernel."""
+    from dense_gemm_sm100_gb300 import gemm
+    M, N, K = shape
+    A, B = inp.make_operands(M, N, K, layout_b=layout, dist="normal", seed=M + 3 * N + K, dtype=mode)
+    g.set_option(gemm.GEMM_OPT_TC_CLUSTER, 1)
+    C1 = run_gpu(g, A, B, layout, mode).cpu()
+    assert "cluster2" not in g.last_path and "pair" not in g.last_path
+    g.set_option(gemm.GEMM_OPT_TC_CLUSTER, cluster_mode)
+    try:
+        C2 = run_gpu(g, A, B, layout, mode).cpu()
+        assert ("cluster2" if cluster_mode == 2 else "pair256x256") in g.last_path
+    finally:
+        g.set_option(gemm.GEMM_OPT_TC_CLUSTER, 3)
+    Cr, S = oracle_of(oracle_mod, A, B, layout)
+    assert_parity(C2, Cr, S, TOL[mode], f"cluster mode {cluster_mode} {mode} {shape}")
+    assert torch.equal(C1, C2)
 
 
 # ------------------------------------------------------- split-K (FP32 path)
