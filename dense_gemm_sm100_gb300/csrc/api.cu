@@ -31,6 +31,7 @@ struct gemm_ctx {
     int split_k = 0;      // 0: chosen per shape; 1: never; n > 1: n K slices (FP32 path)
     int tc_cluster = 3;   // tensor-core mode: 1 one CTA per tile, 2 multicast pairs, 3 pair MMA
     int tc_tma_store = 1; // tensor-core epilogue writes C with TMA stores when C allows it
+    int debug_drop = 0;   // test hook (GEMM_OPT_DEBUG_DROP_LOAD)
 };
 
 namespace {
@@ -260,6 +261,7 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
     lc.status = h->d_status;
     lc.timeout_ns = h->timeout_ns;
     lc.stream = stream;
+    lc.debug_drop = h->debug_drop;
     const char *lay = layout_b == GEMM_B_ROW_MAJOR ? "rowB" : "colB";
     int rc;
     if (dtype == GEMM_F32) {
@@ -513,6 +515,10 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value)
     case GEMM_OPT_SIMT_CONFIG:
         if (value < 0 || value > dg::simt_num_configs()) break;
         h->simt_config = static_cast<int>(value);
+        return GEMM_OK;
+    case GEMM_OPT_DEBUG_DROP_LOAD:
+        if (value != 0 && value != 1) break;
+        h->debug_drop = static_cast<int>(value);
         return GEMM_OK;
     case GEMM_OPT_TC_TMA_STORE:
         if (value != 0 && value != 1) break;

@@ -49,6 +49,7 @@ struct LaunchCommon {
     int grid;             // persistent CTAs to launch
     int group_m;          // tile-order group height (tiles)
     cudaStream_t stream;
+    int debug_drop = 0;   // test hook: CTA 0 skips the copies of its first stage
 };
 
 // Each kernel family raises its dynamic shared-memory limit on the current

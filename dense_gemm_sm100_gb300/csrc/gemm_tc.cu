@@ -64,7 +64,8 @@ struct TcParams {
     int *status;
     unsigned long long timeout_ns;
     int c_vec4;
-    int c_tma;  // 1: C is written by TMA stores through tmC
+    int c_tma;       // 1: C is written by TMA stores through tmC
+    int debug_drop;  // test hook: CTA 0 never loads its first stage
 };
 
 // Unit u of the grouped order over (tile-row groups of CL tiles) x tiles_n:
@@ -189,6 +190,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // A of this CTA, plus all of B: this CTA's half and (CL = 2)
                     // the peer's half, which the peer multicasts here.
                     mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    if (p.debug_drop && blockIdx.x == 0 && it == 0) continue;  // bytes that never come
                     tma_load_2d(a_st, &tmA, fb, kt * BK, mb * BM);
                     if (LAYOUT_B == 0) {
                         if (CL == 1) {
@@ -476,6 +478,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t a_st = sbase + s * P_STAGE_BYTES;
                     const uint32_t b_st = a_st + P_A_BYTES;
                     if (leader) mbar_arrive_expect_tx(fb_local, 2 * P_STAGE_BYTES);
+                    if (p.debug_drop && blockIdx.x == 0 && it == 0) continue;  // bytes that never come
                     tma_load_2d_pair(a_st, &tmA, fb, kt * BK, mb * BM);
                     const int n_half = nb * BN + static_cast<int>(rank) * (BN / 2);
                     if (LAYOUT_B == 0) {
@@ -487,13 +490,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
             }
-            // Every release of the last stages must have landed here before
-            // shared memory goes away (and, after an abort, every copy).
             const uint32_t n = it < (uint32_t)P_STAGES ? it : (uint32_t)P_STAGES;
-            for (uint32_t i = it - n; i < it; ++i) {
-                int dummy = 0;
-                mbar_wait(empty_bar + 8 * (i % P_STAGES), (i / P_STAGES) & 1u, ok ? abort_flag : &dummy,
-                          ok ? p.status : nullptr, kWaitDrain, p.timeout_ns);
+            if (ok) {
+                // Every release of the last stages must have landed here
+                // before shared memory goes away.
+                for (uint32_t i = it - n; i < it; ++i)
+                    mbar_wait(empty_bar + 8 * (i % P_STAGES), (i / P_STAGES) & 1u, abort_flag, p.status,
+                              kWaitDrain, p.timeout_ns);
+            } else if (leader) {
+                // After an abort: the even CTA's full barriers count the copies
+                // of both CTAs; wait (bounded) for those issued last.  The odd
+                // CTA cannot pass the final cluster barrier before this ends.
+                for (uint32_t i = it - n; i < it; ++i) {
+                    int dummy = 0;
+                    mbar_wait(full_bar + 8 * (i % P_STAGES), (i / P_STAGES) & 1u, &dummy, nullptr,
+                              kWaitDrain, p.timeout_ns);
+                }
             }
         }
     } else if (warp == 1) {
@@ -728,6 +740,7 @@ cudaError_t launch_tc(int dtype, int layout_b, const CUtensorMap &tmA, const CUt
     p.timeout_ns = lc.timeout_ns;
     p.c_vec4 = c_vec4 ? 1 : 0;
     p.c_tma = tmC != nullptr ? 1 : 0;
+    p.debug_drop = lc.debug_drop;
     const CUtensorMap &tc = tmC != nullptr ? *tmC : tmA;  // unused when c_tma == 0
     const bool bf16 = dtype == GEMM_BF16;
     if (cl == 3) {

@@ -49,6 +49,7 @@ struct SimtParams {
     int *status;
     unsigned long long timeout_ns;
     int c_vec4;
+    int debug_drop;  // test hook: CTA 0 never loads its first stage
 };
 
 // Work unit u (persistent loop index) -> output tile and K slice.
@@ -164,6 +165,7 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>::TH
                 const uint32_t fb = full_bar + 8 * s;
                 const uint32_t st = sbase + s * STAGE_BYTES;
                 mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                if (p.debug_drop && blockIdx.x == 0 && it == 0) continue;  // bytes that never come
                 tma_load_2d(st, &tmA, fb, kt * BK, mb * BM);
                 if (LAYOUT_B == 0) {
 #pragma unroll
@@ -454,6 +456,7 @@ cudaError_t launch_simt_f32(int config, const CUtensorMap &tmA, const CUtensorMa
     p.status = lc.status;
     p.timeout_ns = lc.timeout_ns;
     p.c_vec4 = p.splits > 1 ? (N % 4 == 0) : (c_vec4 ? 1 : 0);
+    p.debug_drop = lc.debug_drop;
     g_configs[config].launch(layout_b, tmA, tmB, p, lc.grid, lc.stream);
     return cudaGetLastError();
 }

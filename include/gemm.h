@@ -85,6 +85,12 @@ extern "C" {
 #define GEMM_OPT_SPLIT_K 7        /* FP32 K slices: 0 = chosen per shape, 1 = none, 2..64 = forced */
 #define GEMM_OPT_TC_CLUSTER 8     /* tensor-core mode: 1 one CTA per tile, 2 CTA pairs sharing B by multicast, 3 pair MMA (cta_group::2, default) */
 #define GEMM_OPT_TC_TMA_STORE 9   /* 1 (default): tensor-core epilogue stores C by TMA when aligned */
+/* Test hook for failure detection, 0 by default.  1: in the next runs, CTA 0
+ * of the GEMM kernel skips the copies of its first stage while still
+ * expecting their bytes, so every wait that depends on them expires after
+ * GEMM_OPT_WAIT_TIMEOUT_NS; the kernel then leaves C incomplete, ends, and
+ * gemm_sync_status reports GEMM_ERR_TIMEOUT.  The context stays usable. */
+#define GEMM_OPT_DEBUG_DROP_LOAD 10
 
 typedef struct gemm_ctx *gemm_handle_t;
 
