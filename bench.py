@@ -176,7 +176,7 @@ def time_device(run, stream, steps, warmup, counter=None):
     return starts[0].elapsed_time(ends[-1]), per, c1 - c0
 
 
-def bench_workload(g, name, steps, warmup, dist_ctx, peaks, peak_note, with_e2e, sampler=None):
+def bench_workload(g, name, steps, warmup, dist_ctx, peaks, peak_note, with_e2e, side_cublas=False):
     import torch
     from dense_gemm_sm100_gb300 import inputs as inp
     from dense_gemm_sm100_gb300 import roofline as rl
@@ -220,6 +220,20 @@ def bench_workload(g, name, steps, warmup, dist_ctx, peaks, peak_note, with_e2e,
         "launches_timed": launches, "wall_window": (t0, t1),
         "compulsory_bytes": rl.compulsory_bytes(w.M, w.N, w.K, es),
     }
+    if side_cublas:
+        # Labelled side reference: cuBLAS through torch on the same operands,
+        # same stream and power state.  Never part of this library's path.
+        torch.backends.cuda.matmul.allow_tf32 = w.dtype == "tf32"
+        Bl = B_d if w.layout_b == 0 else B_d.t()
+        Af = A_d if w.dtype != "bf16" else A_d
+        cub_ms, _, _ = time_device(lambda: torch.matmul(Af, Bl), stream, max(5, steps // 2), warmup)
+        torch.backends.cuda.matmul.allow_tf32 = False
+        res["cublas_side"] = {
+            "tflops": w.flops / (cub_ms / max(5, steps // 2) * 1e-3) / 1e12,
+            "what": "torch.matmul (cuBLAS) on the same operands; " +
+                    ("BF16 output (cuBLAS default), not FP32" if w.dtype == "bf16" else
+                     "TF32 math allowed" if w.dtype == "tf32" else "FP32, TF32 disallowed"),
+        }
     if with_e2e:
         Ah = A.pin_memory()
         Bh = B.pin_memory()
@@ -346,6 +360,8 @@ def main(argv=None):
     ap.add_argument("--no-modes", action="store_true", help="skip the tensor-core workloads")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-side-reference", action="store_true",
+                    help="skip the labelled cuBLAS side reference")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-s", type=float, default=2.0)
     args = ap.parse_args(argv)
@@ -370,6 +386,11 @@ def main(argv=None):
         sampler.start()
     main_res = bench_workload(g, args.workload, args.steps, args.warmup, ctx, peaks, peak_note,
                               with_e2e=False)
+    side = {}
+    if not args.no_side_reference:
+        side[args.workload] = bench_workload(g, args.workload, min(args.steps, 10), args.warmup, ctx,
+                                             peaks, peak_note, with_e2e=False,
+                                             side_cublas=True)["cublas_side"]
     if sampler:
         sampler.stop()
         clocks = sampler.summary(*main_res["wall_window"])
@@ -380,9 +401,11 @@ def main(argv=None):
             if msampler:
                 msampler.start()
             r = bench_workload(g, name, max(args.steps, 200), args.warmup, ctx, peaks, peak_note,
-                               with_e2e=False)
+                               with_e2e=False, side_cublas=not args.no_side_reference)
             m = {k: r[k] for k in ("workload", "description", "dtype", "value",
                                    "ms_per_step", "kernel_ms", "path", "roofline")}
+            if "cublas_side" in r:
+                m["cublas_side"] = r["cublas_side"]
             if msampler:
                 msampler.stop()
                 m["clocks"] = msampler.summary(*r["wall_window"])
@@ -424,6 +447,7 @@ def main(argv=None):
         "e2e": e2e,
         "cpu_baseline": cpu,
         "modes": modes,
+        "cublas_side": side.get(args.workload),
     }
     print(json.dumps(line))
     return 0

@@ -93,20 +93,29 @@ __device__ __forceinline__ Unit unit_coords(int u, const SimtParams &p)
 // the same bits), halving the FMA instructions the scheduler has to issue.
 // Column-major B keeps scalar FMAs: its B pairs would have to be assembled
 // from two fragments, which costs more issue slots than the packing saves.
+//
+// LAYOUT_B: 0 = row-major B; 1 = column-major B, read transposed from shared
+// memory by the consumers; 2 = column-major B turned in shared memory by the
+// producer warp ("PMPP Chapter 06", section 1, corner turning): TMA lands the
+// K-contiguous tile, the warp rewrites it in the row-major staging layout,
+// and the consumers run the row-major (packed) inner loop.
 template <int LAYOUT_B, int WM, int WN, int TN, int STAGES, int GU, int F2>
 struct Simt {
     static_assert(WM % 2 == 0, "row interleave pairs warps along M");
     static_assert(TN % 4 == 0 && TN <= 16, "thread tile width");
-    static_assert(LAYOUT_B == 0 || TN <= 8, "column-major B uses at most 8 columns per thread");
+    static_assert(LAYOUT_B != 1 || TN <= 8, "column-major B uses at most 8 columns per thread");
     static_assert(8 % GU == 0, "k groups per iteration");
     static constexpr int BM = WM * 32;
     static constexpr int BN = WN * 8 * TN;
+    static_assert(LAYOUT_B != 2 || BN == 128, "the corner-turn lane mapping covers 128 columns");
     static constexpr int A_BYTES = BM * 128;
     static constexpr int B_BYTES = BN * 128;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int LAND_BYTES = LAYOUT_B == 2 ? BN * 128 : 0;  // K-major landing zone
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + LAND_BYTES;
+    static constexpr int NBAR = LAYOUT_B == 2 ? 3 : 2;  // full, empty (, ready)
     static constexpr int CONSUMER_WARPS = WM * WN;
     static constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 2 * STAGES * 8 + 16;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NBAR * STAGES * 8 + 16;
     static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
     static_assert(BM <= 256 && BN <= 256, "TMA box limit");
 };
@@ -125,10 +134,13 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>::TH
     const uint32_t pad = ((raw_addr + 1023u) & ~1023u) - raw_addr;
     uint8_t *smem = smem_raw + pad;
     const uint32_t sbase = raw_addr + pad;
+    constexpr int RL = LAYOUT_B == 2 ? 0 : LAYOUT_B;  // layout the consumers read
+    constexpr int LAND = A_BYTES + S::B_BYTES;        // landing zone offset (LAYOUT_B == 2)
     const uint32_t full_bar = sbase + STAGES * STAGE_BYTES;  // STAGES x 8 bytes
     const uint32_t empty_bar = full_bar + STAGES * 8;         // STAGES x 8 bytes
+    const uint32_t ready_bar = empty_bar + STAGES * 8;        // STAGES x 8 bytes (LAYOUT_B == 2)
     volatile int *abort_flag =
-        reinterpret_cast<volatile int *>(smem + STAGES * STAGE_BYTES + 2 * STAGES * 8);
+        reinterpret_cast<volatile int *>(smem + STAGES * STAGE_BYTES + S::NBAR * STAGES * 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -138,11 +150,118 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>::TH
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar + 8 * s, 1);
             mbar_init(empty_bar + 8 * s, CONSUMER_WARPS);
+            if (LAYOUT_B == 2) mbar_init(ready_bar + 8 * s, 1);
         }
         *abort_flag = 0;
         fence_barrier_init();
     }
     __syncthreads();
+
+    if (LAYOUT_B == 2 && warp == CONSUMER_WARPS) {
+        // ------------------------------------------- producer + corner turn
+        // Lane 0 keeps the ring STAGES-1 k-tiles ahead; all lanes turn each
+        // landed K-major B tile (rows n, 128 bytes of k) into the row-major
+        // staging layout (4 boxes of 32 k-rows x 32 columns, 128-byte
+        // swizzle) that the consumers read.  Lane (g, t) = (lane/8, lane%8)
+        // moves 4x4 blocks of rows 4*(8g+t)..+3 and k-chunk t ^ r (r < 8):
+        // inside each group of 8 lanes both the 16-byte reads and the 16-byte
+        // writes land on 8 distinct bank groups.
+        uint32_t issued = 0;
+        int iss_unit = blockIdx.x, iss_kt = 0, iss_kt_end = 0, iss_mb = 0, iss_nb = 0;
+        auto iss_load_unit = [&]() {
+            if (iss_unit < num_units) {
+                const Unit w = unit_coords(iss_unit, p);
+                iss_mb = w.mb;
+                iss_nb = w.nb;
+                iss_kt = w.kt_begin;
+                iss_kt_end = w.kt_end;
+            }
+        };
+        // lane 0: issue the next k-tile into its ring slot (bounded wait for the slot)
+        auto issue_next = [&]() -> bool {
+            const uint32_t slot = issued % STAGES;
+            const uint32_t ph = (issued / STAGES) & 1u;
+            if (!mbar_wait(empty_bar + 8 * slot, ph ^ 1u, abort_flag, p.status, kWaitProducerEmpty,
+                           p.timeout_ns))
+                return false;
+            const uint32_t fb = full_bar + 8 * slot;
+            const uint32_t st = sbase + slot * STAGE_BYTES;
+            mbar_arrive_expect_tx(fb, A_BYTES + S::LAND_BYTES);
+            if (!(p.debug_drop && blockIdx.x == 0 && issued == 0)) {
+                tma_load_2d(st, &tmA, fb, iss_kt * BK, iss_mb * BM);
+                tma_load_2d(st + LAND, &tmB, fb, iss_kt * BK, iss_nb * BN);
+            }
+            ++issued;
+            if (++iss_kt >= iss_kt_end) {
+                iss_unit += gridDim.x;
+                iss_load_unit();
+            }
+            return true;
+        };
+        bool ok = true;
+        if (lane == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            iss_load_unit();
+            for (int i = 0; ok && i < STAGES - 1 && iss_unit < num_units; ++i) ok = issue_next();
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        const int tg = lane >> 3, tt = lane & 7;
+        const int nq = 8 * tg + tt;  // rows 4*nq .. 4*nq + 3 of the B tile
+        uint32_t it = 0;
+        for (int unit = blockIdx.x; ok && unit < num_units; unit += gridDim.x) {
+            const Unit w = unit_coords(unit, p);
+            for (int kt = w.kt_begin; ok && kt < w.kt_end; ++kt, ++it) {
+                const uint32_t s = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1u;
+                bool got = true;
+                if (lane == 0)
+                    got = mbar_wait(full_bar + 8 * s, ph, abort_flag, p.status, kWaitConsumerFull,
+                                    p.timeout_ns);
+                if (__shfl_sync(0xffffffffu, got ? 1 : 0, 0) == 0) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *land = smem + s * STAGE_BYTES + LAND;
+                uint8_t *brow = smem + s * STAGE_BYTES + A_BYTES + tg * 4096;
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int c = tt ^ r;  // k chunk: k = 4c .. 4c + 3
+                    float4 v[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int n = 4 * nq + q;
+                        v[q] = *reinterpret_cast<const float4 *>(land + n * 128 + ((c ^ (n & 7)) << 4));
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int k = 4 * c + e;
+                        const float4 o = e == 0 ? make_float4(v[0].x, v[1].x, v[2].x, v[3].x)
+                                       : e == 1 ? make_float4(v[0].y, v[1].y, v[2].y, v[3].y)
+                                       : e == 2 ? make_float4(v[0].z, v[1].z, v[2].z, v[3].z)
+                                                : make_float4(v[0].w, v[1].w, v[2].w, v[3].w);
+                        *reinterpret_cast<float4 *>(brow + k * 128 + ((tt ^ (k & 7)) << 4)) = o;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(ready_bar + 8 * s);
+                    if (iss_unit < num_units) ok = issue_next();
+                }
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            }
+        }
+        if (!ok && lane == 0) {
+            // Leave no copy in flight: wait (bounded) for every stage issued
+            // but not yet turned.
+            for (uint32_t i = it; i < issued; ++i) {
+                int dummy = 0;
+                mbar_wait(full_bar + 8 * (i % STAGES), (i / STAGES) & 1u, &dummy, nullptr, kWaitDrain,
+                          p.timeout_ns);
+            }
+        }
+        return;
+    }
 
     if (warp == CONSUMER_WARPS) {
         // ------------------------------------------------------ producer
@@ -202,8 +321,8 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>::TH
     // Row-major B: columns wn*8*TN + 32*c + 4*lc + {0..3} (c < TN/4), i.e.
     // chunk lc of box wn*TN/4 + c; the chunk's place in row k is lc ^ (k & 7).
     // Column-major B: columns col0 + 8*j with col0 & 7 == lc.
-    const int col0 = LAYOUT_B == 0 ? wn * 8 * TN + 4 * lc : wn * 8 * TN + lc;
-    const uint32_t b_base = LAYOUT_B == 0 ? A_BYTES + wn * (TN / 4) * 4096 : A_BYTES + col0 * 128;
+    const int col0 = RL == 0 ? wn * 8 * TN + 4 * lc : wn * 8 * TN + lc;
+    const uint32_t b_base = RL == 0 ? A_BYTES + wn * (TN / 4) * 4096 : A_BYTES + col0 * 128;
 
     uint32_t it = 0;
     for (int unit = blockIdx.x; unit < num_units; unit += gridDim.x) {
@@ -222,6 +341,9 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>::TH
             if (!mbar_wait(full_bar + 8 * s, ph, abort_flag, p.status, kWaitConsumerFull,
                            p.timeout_ns))
                 return;
+            if (LAYOUT_B == 2 && !mbar_wait(ready_bar + 8 * s, ph, abort_flag, p.status,
+                                            kWaitConsumerFull, p.timeout_ns))
+                return;
             const uint8_t *st = smem + s * STAGE_BYTES;
 #pragma unroll 1
             for (int g0 = 0; g0 < 8; g0 += GU) {
@@ -232,8 +354,8 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>::TH
                     float4 a[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) a[i] = *reinterpret_cast<const float4 *>(ap + i * 1024);
-                    float4 bcol[LAYOUT_B == 0 ? 1 : TN];
-                    if (LAYOUT_B != 0) {
+                    float4 bcol[RL == 0 ? 1 : TN];
+                    if (RL != 0) {
                         const uint8_t *bp = st + b_base + ((g ^ lc) << 4);
 #pragma unroll
                         for (int j = 0; j < TN; ++j) bcol[j] = *reinterpret_cast<const float4 *>(bp + j * 1024);
@@ -242,7 +364,7 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>::TH
                     for (int kk = 0; kk < 4; ++kk) {
                         // b2[jp] = columns (2*jp, 2*jp + 1) of B row k = 4*g + kk.
                         float2 b2[TN / 2];
-                        if (LAYOUT_B == 0) {
+                        if (RL == 0) {
                             const int k = 4 * g + kk;
                             const uint8_t *bp = st + b_base + k * 128 + ((lc ^ (k & 7)) << 4);
 #pragma unroll
@@ -262,7 +384,7 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>::TH
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
-                            if (F2 && LAYOUT_B == 0) {
+                            if (F2 && RL == 0) {
                                 const float2 aa = make_float2(av, av);
 #pragma unroll
                                 for (int jp = 0; jp < TN / 2; ++jp) acc2[i][jp] = __ffma2_rn(aa, b2[jp], acc2[i][jp]);
@@ -291,7 +413,7 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>::TH
             const long long m = m_base + 8 * i;
             if (m >= p.M) continue;
             float *crow = cbase + m * p.ldc;
-            if (LAYOUT_B == 0) {
+            if (RL == 0) {
                 // columns 32*c + {0..3}: pairs 2c and 2c + 1
 #pragma unroll
                 for (int c = 0; c < TN / 4; ++c) {
@@ -339,15 +461,24 @@ cudaError_t prepare_one(int *ctas)
     return e;
 }
 
-// Row-major B runs the table's TN; column-major B runs min(TN, 8).
+// Row-major B runs the table's TN; column-major B runs min(TN, 8).  A packed
+// configuration whose column-major tile is 128 wide turns B in shared memory
+// (layout 2, at most 4 stages of 48 KB); the others read it transposed
+// (layout 1).
 constexpr int col_tn(int tn) { return tn < 8 ? tn : 8; }
+constexpr int col_layout(int wn, int tn, int f2) { return (f2 && wn * 8 * col_tn(tn) == 128) ? 2 : 1; }
+constexpr int col_stages(int wn, int tn, int f2, int st)
+{
+    return col_layout(wn, tn, f2) == 2 && st > 4 ? 4 : st;
+}
 
 template <int WM, int WN, int TN, int ST, int GU, int F2>
 cudaError_t prepare_cfg(int *ctas)
 {
     int c0 = 0, c1 = 0;
     cudaError_t e = prepare_one<0, WM, WN, TN, ST, GU, F2>(&c0);
-    if (e == cudaSuccess) e = prepare_one<1, WM, WN, col_tn(TN), ST, GU, F2>(&c1);
+    if (e == cudaSuccess)
+        e = prepare_one<col_layout(WN, TN, F2), WM, WN, col_tn(TN), col_stages(WN, TN, F2, ST), GU, F2>(&c1);
     *ctas = c0 < c1 ? c0 : c1;
     return e;
 }
@@ -360,8 +491,9 @@ void launch_cfg(int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB, co
         using S = Simt<0, WM, WN, TN, ST, GU, F2>;
         sgemm_simt_kernel<0, WM, WN, TN, ST, GU, F2><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
     } else {
-        using S = Simt<1, WM, WN, col_tn(TN), ST, GU, F2>;
-        sgemm_simt_kernel<1, WM, WN, col_tn(TN), ST, GU, F2><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
+        constexpr int L = col_layout(WN, TN, F2), CST = col_stages(WN, TN, F2, ST);
+        using S = Simt<L, WM, WN, col_tn(TN), CST, GU, F2>;
+        sgemm_simt_kernel<L, WM, WN, col_tn(TN), CST, GU, F2><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
     }
 }
 
