@@ -319,6 +319,64 @@ def all_gather_max(ctx, value: float):
     return [float(x.item()) for x in out]
 
 
+# ---------------------------------------------------------------- ladder
+
+# "GEMM 性能优化", 八个台阶: each step's share of cuBLAS on the page's (V100)
+# hardware, as ranges in percent.  Context for the GB300 measurements.
+PAGES_LADDER_PCT = {1: (6, 11), 2: (25, 40), 3: (50, 65), 4: (60, 75), 5: (70, 80),
+                    6: (80, 87), 7: (90, 97)}
+
+
+def run_ladder(args):
+    """Time every kernel of the labelled ladder suite (include/gemm_ladder.h),
+    this library's FP32 path and cuBLAS SGEMM (TF32 off) on one square
+    problem; report TFLOP/s and the share of cuBLAS."""
+    import torch
+    from dense_gemm_sm100_gb300 import gemm
+    from dense_gemm_sm100_gb300 import inputs as inp
+    n = args.ladder_size
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    flops = 2.0 * n * n * n
+    steps = max(1, min(args.steps, 10))
+    A, B = inp.make_operands(n, n, n, seed=3)
+    _, Bc = inp.make_operands(n, n, n, layout_b=inp.B_COL_MAJOR, seed=3)
+    A, B, Bc = A.to(dev), B.to(dev), Bc.to(dev)
+    C = torch.empty((n, n), device=dev)
+
+    def tf(run):
+        _, per, _ = time_device(run, stream, steps, args.warmup)
+        return flops / (statistics.median(per) * 1e-3) / 1e12
+
+    torch.backends.cuda.matmul.allow_tf32 = False
+    cublas = tf(lambda: torch.matmul(A, B))
+    g = gemm.Gemm(0)
+    lib = tf(lambda: g.run(A, B, C, "row", "f32", stream))
+    rows = []
+    for step in [int(x) for x in args.ladder_steps.split(",")]:
+        Bs = Bc if step == gemm.GEMM_LADDER_PMPP_CORNER_TURN else B
+        rc = gemm.gemm_ladder_run(step, n, n, n, A.data_ptr(), Bs.data_ptr(), C.data_ptr(),
+                                  stream.cuda_stream)
+        if rc != gemm.GEMM_OK:
+            rows.append({"step": step, "error": gemm.gemm_status_string(rc)})
+            continue
+        t = tf(lambda: gemm.gemm_ladder_run(step, n, n, n, A.data_ptr(), Bs.data_ptr(),
+                                            C.data_ptr(), stream.cuda_stream))
+        row = {"step": step, "name": gemm.gemm_ladder_name(step), "tflops": round(t, 2),
+               "pct_of_cublas": round(100 * t / cublas, 1)}
+        if step in PAGES_LADDER_PCT:
+            row["pages_pct_of_cublas_v100"] = PAGES_LADDER_PCT[step]
+        rows.append(row)
+    g.close()
+    print(json.dumps({
+        "ladder": rows, "size": n, "unit": UNIT,
+        "library_fp32": {"tflops": round(lib, 2), "pct_of_cublas": round(100 * lib / cublas, 1),
+                         "path": "gemm_run FP32 (TMA + mbarrier + packed FMA)"},
+        "cublas_fp32": {"tflops": round(cublas, 2), "what": "torch.matmul, TF32 disallowed (side reference)"},
+    }))
+    return 0
+
+
 # ---------------------------------------------------------------- entry
 
 def run_reference(args, ctx):
@@ -362,6 +420,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-side-reference", action="store_true",
                     help="skip the labelled cuBLAS side reference")
+    ap.add_argument("--ladder", action="store_true",
+                    help="time the labelled ladder suite (pages' optimisation steps) instead")
+    ap.add_argument("--ladder-size", type=int, default=4096)
+    ap.add_argument("--ladder-steps", default="1,2,3,4,5,6,7,8,101,102")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-s", type=float, default=2.0)
     args = ap.parse_args(argv)
@@ -371,6 +433,8 @@ def main(argv=None):
     ctx = dist_setup()
     if args.impl == "reference":
         return run_reference(args, ctx)
+    if args.ladder:
+        return run_ladder(args)
 
     import torch
     from dense_gemm_sm100_gb300 import gemm

@@ -3,8 +3,9 @@
 The functions ``gemm_create``, ``gemm_run``, ``gemm_run_host``,
 ``gemm_destroy``, ``gemm_validate``, ``gemm_sync_status``,
 ``gemm_set_option``, ``gemm_last_error_string``, ``gemm_status_string``,
-``gemm_last_path``, ``gemm_launch_count``, ``gemm_version`` and
-``gemm_run_noalloc`` take and return
+``gemm_last_path``, ``gemm_launch_count``, ``gemm_version``,
+``gemm_run_noalloc``, ``gemm_ladder_run`` and ``gemm_ladder_name`` take and
+return
 the same plain values as their C counterparts (pointers as ints).  ``Gemm``
 wraps a handle for torch tensors.  Every GEMM step runs in the library's CUDA
 kernels; there is no other code path, and calling anything here without the
@@ -90,6 +91,8 @@ def load_library():
             "gemm_launch_count": ([vp], i64),
             "gemm_version": ([], ci),
             "gemm_run_noalloc": ([ci, i64, i64, i64, vp, i64, vp, i64, vp, i64, ci, vp], ci),
+            "gemm_ladder_run": ([ci, i64, i64, i64, vp, vp, vp, vp], ci),
+            "gemm_ladder_name": ([ci], ctypes.c_char_p),
         }
         for name, (argtypes, restype) in sig.items():
             fn = getattr(lib, name)
@@ -163,6 +166,21 @@ def gemm_run_noalloc(layout_b, M, N, K, A, lda, B, ldb, C, ldc, dtype, stream) -
 
 
 GEMM_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+
+# Labelled benchmark suite (include/gemm_ladder.h): the pages' optimisation
+# ladder and the PMPP worked kernels.  Not the library's GEMM path.
+GEMM_LADDER_STEPS = {1: "naive", 2: "smem_tiling", 3: "thread_tiling", 4: "vectorized",
+                     5: "conflict_free", 6: "warp_tiling", 7: "double_buffer", 8: "cp_async"}
+GEMM_LADDER_PMPP_CORNER_TURN = 101
+GEMM_LADDER_PMPP_COARSENED = 102
+
+
+def gemm_ladder_run(step, M, N, K, A, B, C, stream) -> int:
+    return load_library().gemm_ladder_run(step, M, N, K, A, B, C, stream)
+
+
+def gemm_ladder_name(step) -> str:
+    return load_library().gemm_ladder_name(step).decode()
 
 
 # ------------------------------------------------------------- torch wrapper

@@ -9,6 +9,7 @@ import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gemm.h")
+HEADERS = [HEADER, os.path.join(ROOT, "include", "gemm_ladder.h")]
 
 
 @pytest.fixture(scope="module")
@@ -19,15 +20,18 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(gemm_[a-z_]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b(gemm_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_abi():
     names = declared_functions()
     for required in ("gemm_create", "gemm_run", "gemm_destroy", "gemm_run_host",
-                     "gemm_validate", "gemm_sync_status", "gemm_last_error_string"):
+                     "gemm_validate", "gemm_sync_status", "gemm_last_error_string",
+                     "gemm_run_noalloc", "gemm_ladder_run"):
         assert required in names
 
 
@@ -84,6 +88,18 @@ def test_create_without_gpu_reports_device_error(lib):
     h = ctypes.c_void_p()
     assert lib.gemm_create(ctypes.byref(h), 0) == g.GEMM_ERR_DEVICE
     assert h.value is None
+
+
+def test_ladder_rejects_bad_shapes_without_gpu(lib):
+    from dense_gemm_sm100_gb300 import gemm as g
+    # argument and shape checks happen before any launch
+    assert g.gemm_ladder_run(3, 100, 128, 64, P, P, P, None) == g.GEMM_ERR_INVALID  # M % 128
+    assert g.gemm_ladder_run(102, 64, 100, 64, P, P, P, None) == g.GEMM_ERR_INVALID  # N % 128
+    assert g.gemm_ladder_run(5, 128, 128, 8, P + 4, P, P, None) == g.GEMM_ERR_ALIGNMENT
+    assert g.gemm_ladder_run(999, 128, 128, 8, P, P, P, None) == g.GEMM_ERR_INVALID
+    assert g.gemm_ladder_run(1, 0, 4, 4, P, P, P, None) == g.GEMM_ERR_INVALID
+    assert g.gemm_ladder_name(2).startswith("2 shared-memory tiling")
+    assert g.gemm_ladder_name(77) == ""
 
 
 def test_null_handle_calls_are_rejected(lib):
