@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
@@ -32,6 +33,10 @@ struct gemm_ctx {
     int tc_cluster = 3;   // tensor-core mode: 1 one CTA per tile, 2 multicast pairs, 3 pair MMA
     int tc_tma_store = 1; // tensor-core epilogue writes C with TMA stores when C allows it
     int debug_drop = 0;   // test hook (GEMM_OPT_DEBUG_DROP_LOAD)
+    // gemm_run_host pipeline: copy streams and events (created on first use)
+    cudaStream_t copy_in = nullptr, copy_out = nullptr;
+    cudaEvent_t ev_start = nullptr, ev_done = nullptr;
+    cudaEvent_t ev_a[16] = {}, ev_b[8] = {}, ev_c[16 * 8] = {};  // row panels, column panels, blocks
 };
 
 namespace {
@@ -386,6 +391,16 @@ int gemm_destroy(gemm_handle_t h)
         cudaDeviceSynchronize();
         if (h->ws) cudaFree(h->ws);
         if (h->d_status) cudaFree(h->d_status);
+        if (h->copy_in) cudaStreamDestroy(h->copy_in);
+        if (h->copy_out) cudaStreamDestroy(h->copy_out);
+        for (cudaEvent_t ev : {h->ev_start, h->ev_done})
+            if (ev) cudaEventDestroy(ev);
+        for (cudaEvent_t ev : h->ev_a)
+            if (ev) cudaEventDestroy(ev);
+        for (cudaEvent_t ev : h->ev_b)
+            if (ev) cudaEventDestroy(ev);
+        for (cudaEvent_t ev : h->ev_c)
+            if (ev) cudaEventDestroy(ev);
     }
     delete h;
     return GEMM_OK;
@@ -414,6 +429,148 @@ int gemm_run(gemm_handle_t h, int layout_b, int64_t M, int64_t N, int64_t K, con
     return run_device(h, layout_b, M, N, K, A, lda, B, ldb, C, ldc, dtype, stream, pp, 0);
 }
 
+namespace {
+
+constexpr int kMaxRowPanels = 16, kMaxColPanels = 8;
+
+int ensure_pipeline(gemm_ctx *h)
+{
+    if (h->copy_in) return GEMM_OK;
+    cudaError_t e = cudaStreamCreateWithFlags(&h->copy_in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->copy_out, cudaStreamNonBlocking);
+    for (cudaEvent_t *ev : {&h->ev_start, &h->ev_done})
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    const auto create = [&](cudaEvent_t *evs, int n) {
+        for (int i = 0; i < n && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&evs[i], cudaEventDisableTiming);
+    };
+    create(h->ev_a, kMaxRowPanels);
+    create(h->ev_b, kMaxColPanels);
+    create(h->ev_c, kMaxRowPanels * kMaxColPanels);
+    return e == cudaSuccess ? GEMM_OK : cuda_fail(h, e, "creating the host-copy pipeline");
+}
+
+int64_t gcd64(int64_t a, int64_t b)
+{
+    while (b) {
+        const int64_t t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+// How gemm_run_host cuts C into blocks: the first pm-1 row panels of A
+// (rows each) times pn column panels of B (cols each), one launch per block,
+// then the last row panel times all of B in one launch.  With pm == 1 the
+// only row panel is cut into the pn column blocks.
+struct HostBlocks {
+    int64_t rows = 0, cols = 0;
+    int pm = 1, pn = 1;
+};
+
+// Output tile, tile slots of one persistent wave, for the kernel the
+// problem will run on.
+void tile_shape(const gemm_ctx *h, int layout_b, int64_t M, int64_t N, int dtype, int64_t *bm, int64_t *bn,
+                int64_t *slots, int64_t *full_slots)
+{
+    if (dtype == GEMM_F32) {
+        const int cfg = h->simt_config > 0 ? h->simt_config - 1 : dg::simt_pick_config(M, N, h->sm_count);
+        const dg::SimtTile t = dg::simt_tile(cfg, layout_b);
+        *bm = t.bm;
+        *bn = t.bn;
+        *full_slots = int64_t{h->sm_count} * t.ctas_per_sm;
+        *slots = h->max_ctas > 0 ? h->max_ctas : *full_slots;
+    } else {
+        const bool pair = h->tc_cluster >= 2;
+        const int64_t ctas = h->max_ctas > 0 ? h->max_ctas : h->sm_count;
+        *bm = pair ? 2 * dg::kTcBM : dg::kTcBM;  // a pair covers two tile rows
+        *bn = dg::kTcBN;
+        *slots = pair ? ctas / 2 : ctas;
+        *full_slots = pair ? h->sm_count / 2 : h->sm_count;
+    }
+    if (*slots < 1) *slots = 1;
+    if (*full_slots < *slots) *full_slots = *slots;
+}
+
+// Blocks for the host-buffer pipeline.  While one block runs, the copy of
+// the operand panels of the next in and of the previous block's C out proceed
+// on their own streams, so only the first block's operands and the last
+// launch's C are not hidden.  Blocks of the first row panels are whole
+// persistent waves, at least two ("GEMM 性能优化", Wave 模型); the last row
+// panel spans all columns, so its partial wave is shared as in one call.  No
+// launch is cut along K (that would round differently from the one-call
+// result).  Candidates: one block, and 1, 2, 4 or 8 column panels; the one
+// with the least estimated time wins.
+HostBlocks plan_host_blocks(const gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, int dtype,
+                            int64_t lda_d, int64_t ldb_d)
+{
+    HostBlocks best;
+    best.rows = M;
+    best.cols = N;
+    const auto splits_k = [&](int64_t mp, int64_t np) {
+        return plan_pack(h, layout_b, mp, np, K, nullptr, lda_d, nullptr, ldb_d, dtype).split.splits > 1;
+    };
+    if (K == 0 || splits_k(M, N)) return best;
+    const int es = elem_bytes(dtype);
+    int64_t bm, bn, slots, full_slots;
+    tile_shape(h, layout_b, M, N, dtype, &bm, &bn, &slots, &full_slots);
+    const auto waves = [&](int64_t mp, int64_t np) {
+        const int64_t tiles = ((mp + bm - 1) / bm) * ((np + bn - 1) / bn);
+        return (tiles + slots - 1) / slots;
+    };
+    // Rough rates of these kernels on all SMs and of the host link; they only
+    // rank plans.  A wave takes as long with fewer slots (GEMM_OPT_MAX_CTAS).
+    const double rate = dtype == GEMM_F32 ? 64e12 : dtype == GEMM_TF32 ? 800e12 : 1650e12;  // FLOP/s
+    const double link = 200e9;                                                             // bytes/s each way
+    const double wave_s = 2.0 * bm * bn * K * full_slots / rate;
+    const double h2d_all = (double(M) * K + double(K) * N) * es, d2h_all = double(M) * N * 4;
+    const auto estimate = [&](int64_t w, int launches, double head, double tail) {
+        const double body = std::max({w * wave_s, (h2d_all - head) / link, (d2h_all - tail) / link});
+        return head / link + body + tail / link + launches * 10e-6;
+    };
+    double best_s = estimate(waves(M, N), 1, h2d_all, d2h_all);
+    for (int pn_try = 1; pn_try <= kMaxColPanels; pn_try *= 2) {
+        const int64_t cols = round_up((N + pn_try - 1) / pn_try, bn);
+        const int pn = static_cast<int>((N + cols - 1) / cols);
+        if (pn != pn_try) continue;
+        const int64_t last_cols = N - (pn - 1) * cols;
+        const int64_t tiles_n = cols / bn;
+        int64_t unit = slots / gcd64(slots, tiles_n);  // fewest tile rows that fill whole waves
+        if (unit > 64) {
+            if (pn > 1) continue;  // column panels only where waves come out whole
+            unit = 1;
+        }
+        int64_t bands = unit;
+        while (bands * tiles_n < 2 * slots) bands += unit;
+        int64_t rows = bands * bm;
+        if ((M + rows - 1) / rows > kMaxRowPanels) rows = round_up((M + kMaxRowPanels - 1) / kMaxRowPanels, unit * bm);
+        while (rows < M && (splits_k(rows, cols) || splits_k(rows, last_cols))) rows += bm;
+        if (rows >= M) rows = M;
+        int pm = static_cast<int>((M + rows - 1) / rows);
+        if (pm > 1 && splits_k(M - (pm - 1) * rows, N)) --pm;  // a small last panel joins the one before it
+        if (pm == 1 && pn == 1) continue;                        // the one-block plan, estimated above
+        if (pm == 1 && (splits_k(M, cols) || splits_k(M, last_cols))) continue;
+        const int64_t last_rows = M - (pm - 1) * rows;
+        const int64_t panel_rows = pm > 1 ? rows : M;
+        int64_t w = int64_t{pm > 1 ? pm - 1 : 1} * ((pn - 1) * waves(panel_rows, cols) + waves(panel_rows, last_cols));
+        if (pm > 1) w += waves(last_rows, N);
+        const int launches = (pm > 1 ? pm - 1 : 1) * pn + (pm > 1 ? 1 : 0);
+        const double head = (double(panel_rows) + (pn > 1 ? cols : N)) * K * es;
+        const double tail = pm > 1 ? double(last_rows) * N * 4 : double(M) * last_cols * 4;
+        const double t = estimate(w, launches, head, tail);
+        if (t < best_s) {
+            best_s = t;
+            best.rows = panel_rows;
+            best.cols = cols;
+            best.pm = pm;
+            best.pn = pn;
+        }
+    }
+    return best;
+}
+
+}  // namespace
+
 int gemm_run_host(gemm_handle_t h, int layout_b, int64_t M, int64_t N, int64_t K, const void *A_host,
                   int64_t lda, const void *B_host, int64_t ldb, float *C_host, int64_t ldc,
                   int dtype, cudaStream_t stream)
@@ -427,10 +584,13 @@ int gemm_run_host(gemm_handle_t h, int layout_b, int64_t M, int64_t N, int64_t K
         return GEMM_OK;
     }
     DeviceGuard guard(h->device);
+    rc = ensure_pipeline(h);
+    if (rc) return rc;
     const int es = elem_bytes(dtype);
+    const bool b_row = layout_b == GEMM_B_ROW_MAJOR;
     const int64_t al = 16 / es;
-    const int64_t rows_b = layout_b == GEMM_B_ROW_MAJOR ? K : N;
-    const int64_t cols_b = layout_b == GEMM_B_ROW_MAJOR ? N : K;
+    const int64_t rows_b = b_row ? K : N;
+    const int64_t cols_b = b_row ? N : K;
     const int64_t lda_d = K ? round_up(K, al) : 0;
     const int64_t ldb_d = K ? round_up(cols_b, al) : 0;
     const int64_t ldc_d = round_up(N, 4);
@@ -438,35 +598,91 @@ int gemm_run_host(gemm_handle_t h, int layout_b, int64_t M, int64_t N, int64_t K
     const size_t b_bytes = static_cast<size_t>(round_up(rows_b * ldb_d * es, 256));
     const size_t c_bytes = static_cast<size_t>(round_up(M * ldc_d * 4, 256));
     const size_t staged = a_bytes + b_bytes + c_bytes;
-    // Pointers are only needed for the alignment test of the pack plan; the
-    // staged buffers below are 256-byte aligned with 16-byte-multiple rows.
-    rc = ensure_workspace(h, staged);
+
+    const HostBlocks hb = plan_host_blocks(h, layout_b, M, N, K, dtype, lda_d, ldb_d);
+    const auto block_m = [&](int i) { return i == hb.pm - 1 ? M - i * hb.rows : hb.rows; };
+    const auto block_n = [&](int j) { return j == hb.pn - 1 ? N - j * hb.cols : hb.cols; };
+    // The staged buffers are 256-byte aligned with 16-byte-multiple rows and
+    // block offsets, so no block needs a re-pack; only split-K partials (of a
+    // problem too small to be cut into blocks) may need room.
+    const size_t extra = plan_pack(h, layout_b, block_m(0), block_n(0), K, nullptr, lda_d, nullptr, ldb_d, dtype).total();
+    rc = ensure_workspace(h, staged + extra);
     if (rc) return rc;
     uint8_t *ws = static_cast<uint8_t *>(h->ws);
-    void *A_d = ws, *B_d = ws + a_bytes;
+    uint8_t *A_d = ws, *B_d = ws + a_bytes;
     float *C_d = reinterpret_cast<float *>(ws + a_bytes + b_bytes);
-    const PackPlan pp = plan_pack(h, layout_b, M, N, K, A_d, lda_d, B_d, ldb_d, dtype);
-    if (pp.total()) {
-        rc = ensure_workspace(h, staged + pp.total());  // may move the buffer: recompute below
-        if (rc) return rc;
-        ws = static_cast<uint8_t *>(h->ws);
-        A_d = ws;
-        B_d = ws + a_bytes;
-        C_d = reinterpret_cast<float *>(ws + a_bytes + b_bytes);
+    const uint8_t *A_h = static_cast<const uint8_t *>(A_host);
+    const uint8_t *B_h = static_cast<const uint8_t *>(B_host);
+
+    // Column panel j of B: columns j*cols.. of a row-major K x N matrix, or
+    // rows j*cols.. of the column-major (N x K) storage.
+    const auto b_offset_d = [&](int j) { return b_row ? j * hb.cols * es : j * hb.cols * ldb_d * es; };
+    const auto copy_b = [&](int j) {
+        const int64_t nj = block_n(j);
+        if (b_row)
+            return cudaMemcpy2DAsync(B_d + b_offset_d(j), ldb_d * es, B_h + j * hb.cols * es, ldb * es, nj * es, K,
+                                     cudaMemcpyHostToDevice, h->copy_in);
+        return cudaMemcpy2DAsync(B_d + b_offset_d(j), ldb_d * es, B_h + j * hb.cols * ldb * es, ldb * es, K * es,
+                                 nj, cudaMemcpyHostToDevice, h->copy_in);
+    };
+    const auto copy_a = [&](int i) {
+        return cudaMemcpy2DAsync(A_d + i * hb.rows * lda_d * es, lda_d * es, A_h + i * hb.rows * lda * es, lda * es,
+                                 K * es, block_m(i), cudaMemcpyHostToDevice, h->copy_in);
+    };
+
+    cudaError_t e = cudaEventRecord(h->ev_start, stream);  // after earlier work on the stream
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->copy_in, h->ev_start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->copy_out, h->ev_start, 0);
+    if (e != cudaSuccess) return cuda_fail(h, e, "host-copy pipeline set-up");
+    // Copies in: B_0, A_0 .. A_{pm-1}, B_1 .. B_{pn-1}.  Launches: the blocks
+    // of the first row panels column panel by column panel, each waiting only
+    // for its own two panels, then the last row panel across all columns.
+    std::string path;
+    int block = 0;
+    const auto launch = [&](int64_t m0, int64_t n0, int64_t mi, int64_t nj) {
+        uint8_t *A_p = A_d + m0 * lda_d * es;
+        uint8_t *B_p = B_d + (b_row ? n0 * es : n0 * ldb_d * es);
+        float *C_p = C_d + m0 * ldc_d + n0;
+        const PackPlan pp = plan_pack(h, layout_b, mi, nj, K, A_p, lda_d, B_p, ldb_d, dtype);
+        int r = run_device(h, layout_b, mi, nj, K, A_p, lda_d, B_p, ldb_d, C_p, ldc_d, dtype, stream, pp, staged);
+        if (r) return r;
+        if (block == 0) path = h->last_path;
+        cudaError_t err = cudaEventRecord(h->ev_c[block], stream);
+        if (err == cudaSuccess) err = cudaStreamWaitEvent(h->copy_out, h->ev_c[block], 0);
+        if (err == cudaSuccess)
+            err = cudaMemcpy2DAsync(C_host + m0 * ldc + n0, ldc * 4, C_p, ldc_d * 4, nj * 4, mi,
+                                    cudaMemcpyDeviceToHost, h->copy_out);
+        ++block;
+        return err == cudaSuccess ? GEMM_OK : cuda_fail(h, err, "copy of C to the host");
+    };
+    const auto wait_copy = [&](cudaError_t err, cudaEvent_t ev, const char *what) {
+        if (err == cudaSuccess) err = cudaEventRecord(ev, h->copy_in);
+        if (err == cudaSuccess) err = cudaStreamWaitEvent(stream, ev, 0);
+        return err == cudaSuccess ? GEMM_OK : cuda_fail(h, err, what);
+    };
+    const int blocked_panels = hb.pm > 1 ? hb.pm - 1 : 1;
+    for (int j = 0; j < hb.pn; ++j) {
+        if (K > 0 && (rc = wait_copy(copy_b(j), h->ev_b[j], "copy of B to the device"))) return rc;
+        for (int i = 0; i < blocked_panels; ++i) {
+            if (K > 0 && j == 0 && (rc = wait_copy(copy_a(i), h->ev_a[i], "copy of A to the device"))) return rc;
+            if ((rc = launch(i * hb.rows, j * hb.cols, block_m(i), block_n(j)))) return rc;
+        }
+        if (K > 0 && j == 0 && hb.pm > 1) {  // A's last panel, before the rest of B
+            e = copy_a(hb.pm - 1);
+            if (e == cudaSuccess) e = cudaEventRecord(h->ev_a[hb.pm - 1], h->copy_in);
+            if (e != cudaSuccess) return cuda_fail(h, e, "copy of A to the device");
+        }
     }
-    cudaError_t e;
-    if (K > 0) {
-        e = cudaMemcpy2DAsync(A_d, lda_d * es, A_host, lda * es, K * es, M, cudaMemcpyHostToDevice, stream);
-        if (e != cudaSuccess) return cuda_fail(h, e, "copy of A to the device");
-        e = cudaMemcpy2DAsync(B_d, ldb_d * es, B_host, ldb * es, cols_b * es, rows_b,
-                              cudaMemcpyHostToDevice, stream);
-        if (e != cudaSuccess) return cuda_fail(h, e, "copy of B to the device");
+    if (hb.pm > 1) {
+        if (K > 0 && (e = cudaStreamWaitEvent(stream, h->ev_a[hb.pm - 1], 0)) != cudaSuccess)
+            return cuda_fail(h, e, "copy of A to the device");
+        if ((rc = launch((hb.pm - 1) * hb.rows, 0, block_m(hb.pm - 1), N))) return rc;
     }
-    rc = run_device(h, layout_b, M, N, K, A_d, lda_d, B_d, ldb_d, C_d, ldc_d, dtype, stream, pp, staged);
-    if (rc) return rc;
-    e = cudaMemcpy2DAsync(C_host, ldc * 4, C_d, ldc_d * 4, N * 4, M, cudaMemcpyDeviceToHost, stream);
-    if (e != cudaSuccess) return cuda_fail(h, e, "copy of C to the host");
-    h->last_path = "host+" + h->last_path;
+    e = cudaEventRecord(h->ev_done, h->copy_out);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, h->ev_done, 0);  // the call ends on `stream`
+    if (e != cudaSuccess) return cuda_fail(h, e, "host-copy pipeline completion");
+    h->last_path = "host+" + path;
+    if (block > 1) h->last_path += "+blocks" + std::to_string(hb.pm) + "x" + std::to_string(hb.pn);  // launches: (pm-1)*pn+1
     return GEMM_OK;
 }
 

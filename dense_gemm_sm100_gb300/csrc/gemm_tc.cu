@@ -717,7 +717,7 @@ int tc_grid(int64_t M, int64_t N, int sm_count, int cluster)
     const int64_t tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
     const int cl = cluster >= 2 ? 2 : 1;
     const int64_t units = ((tiles_m + cl - 1) / cl) * tiles_n;
-    const int64_t clusters = sm_count / cl;
+    const int64_t clusters = sm_count >= cl ? sm_count / cl : 1;
     return static_cast<int>(cl * (units < clusters ? units : clusters));
 }
 

@@ -120,12 +120,18 @@ int gemm_run(gemm_handle_t h, int layout_b, int64_t M, int64_t N, int64_t K,
              float *C, int64_t ldc, int dtype, cudaStream_t stream);
 
 /*
- * As gemm_run, but A, B and C are HOST pointers.  The call copies A and B
- * into the handle's workspace (one cudaMemcpy2DAsync each), runs the GEMM,
- * copies C back (one cudaMemcpy2DAsync), all on `stream`, and returns without
- * waiting: the host buffers must stay valid and C must not be read until the
- * stream has been synchronised.  Pinned (page-locked) host memory makes the
- * copies asynchronous; pageable memory works but the copies block.
+ * As gemm_run, but A, B and C are HOST pointers.  The call stages A and B in
+ * the handle's workspace, runs the GEMM and copies C back, and returns
+ * without waiting: the host buffers must stay valid and C must not be read
+ * until `stream` has been synchronised.  For large problems C is computed in
+ * blocks (row panels of A times column panels of B, each a whole number of
+ * persistent waves), and the copies of the next block's operands in and the
+ * previous block's C out run on two internal streams of the handle while a
+ * block computes; events order the copies after the work already queued on
+ * `stream` and make `stream` wait for the last copy, so the call behaves as
+ * one operation on `stream`.  The result is bit-identical to gemm_run on the
+ * same operands (no block is cut along K).  Pinned (page-locked) host memory
+ * makes the copies asynchronous; pageable memory works but the copies block.
  */
 int gemm_run_host(gemm_handle_t h, int layout_b, int64_t M, int64_t N, int64_t K,
                   const void *A_host, int64_t lda, const void *B_host, int64_t ldb,

@@ -241,6 +241,71 @@ def test_run_host_matches_device(g, mode, layout):
     assert torch.equal(Cd, Ch)
 
 
+@pytest.mark.parametrize("mode,layout,max_ctas,shape,blocks", [
+    ("f32", ROW, 2, (2048, 2048, 256), "2x2"),    # row panels x column panels of B
+    ("f32", COL, 4, (3000, 3000, 256), "6x1"),    # ragged last row panel, all columns
+    ("f32", ROW, 2, (3000, 1000, 256), "2x1"),    # a 440-row rest would be cut along K: joined
+    ("f32", ROW, 2, (10000, 256, 1024), "2x1"),   # panels grow to 4992 rows, none cut along K
+    ("f32", COL, 4, (2000, 1000, 512), "1x1"),    # copies outweigh the compute: one block
+    ("bf16", ROW, 16, (1000, 3000, 256), "1x2"),  # one row panel in two column blocks
+    ("bf16", COL, 8, (1000, 3000, 256), "2x2"),
+    ("bf16", ROW, 8, (3000, 3000, 1024), "6x2"),  # pair MMA blocks
+    ("tf32", COL, 8, (2300, 2000, 512), "5x2"),
+    ("tf32", ROW, 4, (1000, 1000, 512), "2x2"),
+])
+def test_run_host_blocks_match_device(g, mode, layout, max_ctas, shape, blocks):
+    """gemm_run_host cuts C into blocks (row panels of A x column panels of B)
+    whose copies in and out overlap the GEMMs of the neighbouring blocks; the
+    result is bit-identical to one device-resident call, also with host
+    leading dimensions wider than the matrix.  The tile-slot cap shrinks the
+    blocks so that small problems exercise the plan."""
+    from dense_gemm_sm100_gb300 import gemm
+    M, N, K = shape
+    g.set_option(gemm.GEMM_OPT_MAX_CTAS, max_ctas)
+    try:
+        A, B = inp.make_operands(M, N, K, layout_b=layout, seed=M + N, dtype=mode)
+        Cd = run_gpu(g, A, B, layout, mode).cpu()
+        Ap = torch.zeros((M, K + 5), dtype=A.dtype).pin_memory()[:, :K]
+        Ap.copy_(A)
+        Bp = torch.zeros((B.shape[0], B.shape[1] + 7), dtype=B.dtype).pin_memory()[:, :B.shape[1]]
+        Bp.copy_(B)
+        Ch = torch.full((M, N + 3), -1.0).pin_memory()
+        g.run_host(Ap, Bp, Ch[:, :N], layout, mode)
+        g.sync_status()
+        assert g.last_path.startswith("host+")
+        assert ("+blocks" not in g.last_path) if blocks == "1x1" else g.last_path.endswith(f"+blocks{blocks}")
+        assert torch.equal(Cd, Ch[:, :N])
+        assert torch.all(Ch[:, N:] == -1.0)  # nothing written past N
+    finally:
+        g.set_option(gemm.GEMM_OPT_MAX_CTAS, 0)
+
+
+def test_run_host_orders_with_the_callers_stream(g):
+    """The copies of A and B start after work queued earlier on the caller's
+    stream (here: the copy that fills the host buffer of A), and C is
+    complete once that stream is synchronised."""
+    from dense_gemm_sm100_gb300 import gemm
+    g.set_option(gemm.GEMM_OPT_MAX_CTAS, 2)
+    try:
+        s = torch.cuda.Stream()
+        M, N, K = 2048, 2048, 256
+        A, B = inp.make_operands(M, N, K, seed=7)
+        A_d = A.cuda()
+        Cd = run_gpu(g, A, B, ROW, "f32").cpu()
+        for _ in range(3):
+            Ap = torch.zeros((M, K)).pin_memory()
+            Ch = torch.zeros((M, N)).pin_memory()
+            with torch.cuda.stream(s):
+                torch.cuda._sleep(2_000_000)  # keep the stream busy before the fill
+                Ap.copy_(A_d, non_blocking=True)
+            g.run_host(Ap, B.pin_memory(), Ch, ROW, "f32", stream=s)
+            s.synchronize()
+            assert g.last_path.endswith("+blocks2x2")
+            assert torch.equal(Cd, Ch)
+    finally:
+        g.set_option(gemm.GEMM_OPT_MAX_CTAS, 0)
+
+
 def test_launch_count_increments(g):
     before = g.launch_count
     A, B = inp.make_operands(64, 64, 64, seed=1)
