@@ -46,7 +46,6 @@ NOMINAL_PF = {"bf16": 2.25, "tf32": 1.1}
 # ncu capture of the kernel as it is now; None until captured for this version.
 # Key: workload name -> (bytes per launch, summary file under profiles/).
 NCU_TRAFFIC: dict[str, tuple[float, str]] = {
-    "fp32_8192_row": (3309.6e6 + 261.1e6, "profiles/dram_traffic_full_size.md"),
 }
 
 DESCRIPTIONS = {
@@ -57,6 +56,8 @@ DESCRIPTIONS = {
     "fp32_4095x3073x2047_row": "FP32 SIMT GEMM M=4095 N=3073 K=2047, row-major, N(0,1) seed 2",
     "fp32_128_row": "FP32 SIMT GEMM M=N=K=128, row-major, U[-1,1) seed 0",
     "fp32_4096_row": "FP32 SIMT GEMM M=N=K=4096, row-major, U[-1,1) seed 3 (profiling size)",
+    "fp32_3648x4096x4096_row": "FP32 SIMT GEMM M=3648 N=K=4096, row-major, U[-1,1) seed 3 "
+                               "(profiling size: whole waves of 192x128 tiles)",
     "ffn_bf16_4096x7168x4096": "tensor-core GEMM, BF16, M=4096 N=7168 K=4096 (profiling size)",
     "ffn_tf32_4096x7168x4096": "tensor-core GEMM, TF32, M=4096 N=7168 K=4096 (profiling size)",
 }

@@ -143,18 +143,17 @@ PackPlan plan_pack(const gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_
         pp.b_bytes = static_cast<size_t>(round_up(rows * pp.ldb * es, 256));
     }
     if (dtype == GEMM_F32) {
-        pp.simt_config = h->simt_config > 0 ? h->simt_config - 1 : dg::simt_pick_config(M, N, h->sm_count);
+        pp.simt_config = h->simt_config > 0 ? h->simt_config - 1 : dg::simt_pick_config(M, N, K, layout_b, h->sm_count, h->max_ctas);
+        const dg::SimtTile t = dg::simt_tile(pp.simt_config, layout_b);
         if (h->split_k == 0) {
-            pp.split = dg::simt_pick_splits(pp.simt_config, layout_b, M, N, K, h->sm_count);
-        } else if (h->split_k > 1) {
-            const int64_t k_tiles = (K + dg::kSimtBK - 1) / dg::kSimtBK;
-            const int64_t want = h->split_k < k_tiles ? h->split_k : k_tiles;
-            const int64_t kt_per = (k_tiles + want - 1) / want;
-            pp.split.splits = static_cast<int>((k_tiles + kt_per - 1) / kt_per);
-            pp.split.k_per_split = static_cast<int>(kt_per * dg::kSimtBK);
+            const int64_t slots = h->max_ctas > 0 ? h->max_ctas : int64_t{h->sm_count} * t.ctas_per_sm;
+            pp.split = dg::simt_pick_splits(pp.simt_config, layout_b, M, N, K, slots);
+        } else if (h->split_k > 1) {  // every tile in split_k slices
+            const int64_t tiles = ((M + t.bm - 1) / t.bm) * ((N + t.bn - 1) / t.bn);
+            pp.split = dg::simt_split_k(tiles, tiles, h->split_k, K);
         }
-        if (pp.split.splits > 1)
-            pp.split_bytes = static_cast<size_t>(round_up(int64_t{pp.split.splits} * M * N * 4, 256));
+        pp.split_bytes = static_cast<size_t>(
+            round_up(static_cast<int64_t>(dg::simt_partial_bytes(pp.simt_config, layout_b, pp.split)), 256));
     }
     return pp;
 }
@@ -281,7 +280,7 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
         if (rc) return rc;
         dg::SplitK sk = pp.split;
         if (sk.splits > 1) sk.partials = reinterpret_cast<float *>(ws + pp.a_bytes + pp.b_bytes);
-        const int64_t units = ((M + t.bm - 1) / t.bm) * ((N + t.bn - 1) / t.bn) * sk.splits;
+        const int64_t units = dg::simt_units(cfg, layout_b, M, N, sk);
         const int64_t cap = h->max_ctas > 0 ? h->max_ctas : int64_t{h->sm_count} * t.ctas_per_sm;
         lc.grid = static_cast<int>(units < cap ? units : cap);
         lc.group_m = h->simt_group_m;
@@ -291,9 +290,12 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
         path = std::string("simt_f32_") + t.name + "_" + lay + path;
         if (sk.splits > 1) {
             ++h->launches;
-            e = dg::launch_splitk_reduce(sk.partials, sk.splits, C, ldc, M, N, h->sm_count, stream);
+            e = dg::launch_simt_tail_reduce(cfg, layout_b, static_cast<int>(M), static_cast<int>(N),
+                                            static_cast<int>(K), C, ldc, c_vec4, lc, sk, h->sm_count);
             if (e != cudaSuccess) return cuda_fail(h, e, "split-K reduction launch");
-            path += "+splitk" + std::to_string(sk.splits);
+            const int64_t tiles = ((M + t.bm - 1) / t.bm) * ((N + t.bn - 1) / t.bn);
+            path += sk.tail_tiles == tiles ? "+splitk" + std::to_string(sk.splits)
+                                           : "+tail" + std::to_string(sk.tail_tiles) + "x" + std::to_string(sk.splits);
         }
     } else {
         const int bk = dg::tc_bk(es);
@@ -470,11 +472,12 @@ struct HostBlocks {
 
 // Output tile, tile slots of one persistent wave, for the kernel the
 // problem will run on.
-void tile_shape(const gemm_ctx *h, int layout_b, int64_t M, int64_t N, int dtype, int64_t *bm, int64_t *bn,
-                int64_t *slots, int64_t *full_slots)
+void tile_shape(const gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, int dtype, int64_t *bm,
+                int64_t *bn, int64_t *slots, int64_t *full_slots)
 {
     if (dtype == GEMM_F32) {
-        const int cfg = h->simt_config > 0 ? h->simt_config - 1 : dg::simt_pick_config(M, N, h->sm_count);
+        const int cfg = h->simt_config > 0 ? h->simt_config - 1
+                                           : dg::simt_pick_config(M, N, K, layout_b, h->sm_count, h->max_ctas);
         const dg::SimtTile t = dg::simt_tile(cfg, layout_b);
         *bm = t.bm;
         *bn = t.bn;
@@ -497,23 +500,18 @@ void tile_shape(const gemm_ctx *h, int layout_b, int64_t M, int64_t N, int dtype
 // on their own streams, so only the first block's operands and the last
 // launch's C are not hidden.  Blocks of the first row panels are whole
 // persistent waves, at least two ("GEMM 性能优化", Wave 模型); the last row
-// panel spans all columns, so its partial wave is shared as in one call.  No
-// launch is cut along K (that would round differently from the one-call
-// result).  Candidates: one block, and 1, 2, 4 or 8 column panels; the one
-// with the least estimated time wins.
-HostBlocks plan_host_blocks(const gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, int dtype,
-                            int64_t lda_d, int64_t ldb_d)
+// panel spans all columns, so its partial wave is shared as in one call.
+// Candidates: one block, and 1, 2, 4 or 8 column panels; the one with the
+// least estimated time wins.
+HostBlocks plan_host_blocks(const gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, int dtype)
 {
     HostBlocks best;
     best.rows = M;
     best.cols = N;
-    const auto splits_k = [&](int64_t mp, int64_t np) {
-        return plan_pack(h, layout_b, mp, np, K, nullptr, lda_d, nullptr, ldb_d, dtype).split.splits > 1;
-    };
-    if (K == 0 || splits_k(M, N)) return best;
+    if (K == 0) return best;
     const int es = elem_bytes(dtype);
     int64_t bm, bn, slots, full_slots;
-    tile_shape(h, layout_b, M, N, dtype, &bm, &bn, &slots, &full_slots);
+    tile_shape(h, layout_b, M, N, K, dtype, &bm, &bn, &slots, &full_slots);
     const auto waves = [&](int64_t mp, int64_t np) {
         const int64_t tiles = ((mp + bm - 1) / bm) * ((np + bn - 1) / bn);
         return (tiles + slots - 1) / slots;
@@ -544,12 +542,9 @@ HostBlocks plan_host_blocks(const gemm_ctx *h, int layout_b, int64_t M, int64_t 
         while (bands * tiles_n < 2 * slots) bands += unit;
         int64_t rows = bands * bm;
         if ((M + rows - 1) / rows > kMaxRowPanels) rows = round_up((M + kMaxRowPanels - 1) / kMaxRowPanels, unit * bm);
-        while (rows < M && (splits_k(rows, cols) || splits_k(rows, last_cols))) rows += bm;
         if (rows >= M) rows = M;
-        int pm = static_cast<int>((M + rows - 1) / rows);
-        if (pm > 1 && splits_k(M - (pm - 1) * rows, N)) --pm;  // a small last panel joins the one before it
-        if (pm == 1 && pn == 1) continue;                        // the one-block plan, estimated above
-        if (pm == 1 && (splits_k(M, cols) || splits_k(M, last_cols))) continue;
+        const int pm = static_cast<int>((M + rows - 1) / rows);
+        if (pm == 1 && pn == 1) continue;  // the one-block plan, estimated above
         const int64_t last_rows = M - (pm - 1) * rows;
         const int64_t panel_rows = pm > 1 ? rows : M;
         int64_t w = int64_t{pm > 1 ? pm - 1 : 1} * ((pn - 1) * waves(panel_rows, cols) + waves(panel_rows, last_cols));
@@ -599,13 +594,16 @@ int gemm_run_host(gemm_handle_t h, int layout_b, int64_t M, int64_t N, int64_t K
     const size_t c_bytes = static_cast<size_t>(round_up(M * ldc_d * 4, 256));
     const size_t staged = a_bytes + b_bytes + c_bytes;
 
-    const HostBlocks hb = plan_host_blocks(h, layout_b, M, N, K, dtype, lda_d, ldb_d);
+    const HostBlocks hb = plan_host_blocks(h, layout_b, M, N, K, dtype);
     const auto block_m = [&](int i) { return i == hb.pm - 1 ? M - i * hb.rows : hb.rows; };
     const auto block_n = [&](int j) { return j == hb.pn - 1 ? N - j * hb.cols : hb.cols; };
     // The staged buffers are 256-byte aligned with 16-byte-multiple rows and
-    // block offsets, so no block needs a re-pack; only split-K partials (of a
-    // problem too small to be cut into blocks) may need room.
-    const size_t extra = plan_pack(h, layout_b, block_m(0), block_n(0), K, nullptr, lda_d, nullptr, ldb_d, dtype).total();
+    // block offsets, so no launch needs a re-pack; only split-K partial tiles
+    // need room, as much as the largest of the launches' shapes.
+    size_t extra = 0;
+    for (int64_t mi : {block_m(0), block_m(hb.pm - 1)})
+        for (int64_t nj : {block_n(0), block_n(hb.pn - 1), N})
+            extra = std::max(extra, plan_pack(h, layout_b, mi, nj, K, nullptr, lda_d, nullptr, ldb_d, dtype).total());
     rc = ensure_workspace(h, staged + extra);
     if (rc) return rc;
     uint8_t *ws = static_cast<uint8_t *>(h->ws);
@@ -730,6 +728,7 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value)
         return GEMM_OK;
     case GEMM_OPT_SIMT_CONFIG:
         if (value < 0 || value > dg::simt_num_configs()) break;
+        if (value > 0 && !dg::simt_config_usable(static_cast<int>(value) - 1)) break;
         h->simt_config = static_cast<int>(value);
         return GEMM_OK;
     case GEMM_OPT_DEBUG_DROP_LOAD:

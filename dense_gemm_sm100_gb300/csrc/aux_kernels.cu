@@ -6,8 +6,6 @@
 //    16-byte aligned rows).  One CTA walks whole rows: reads and writes are
 //    both row-contiguous, so every warp access is coalesced ("PMPP Chapter 06:
 //    Performance considerations", section 1, coalescing).
-//  * split-K reduction: C = sum of the K-slice partial products, in slice
-//    order ("GEMM 性能优化", 台阶 1: partial sums over K slices add up to C).
 //  * zero fill: C = 0 for K = 0 (the empty sum).
 #include <cstdint>
 
@@ -37,23 +35,6 @@ __global__ void __launch_bounds__(256) zero_fill_kernel(float *__restrict__ C, l
     }
 }
 
-// One CTA per row (grid-stride); the slices are added in index order.
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restrict__ W, int splits,
-                                                            float *__restrict__ C, long long ldc,
-                                                            long long M, long long N)
-{
-    const long long stride = M * N;
-    for (long long r = blockIdx.x; r < M; r += gridDim.x) {
-        const float *w = W + r * N;
-        float *c = C + r * ldc;
-        for (long long j = threadIdx.x; j < N; j += blockDim.x) {
-            float acc = w[j];
-            for (int s = 1; s < splits; ++s) acc += w[s * stride + j];
-            c[j] = acc;
-        }
-    }
-}
-
 int rows_grid(long long rows, int sm_count)
 {
     const long long cap = static_cast<long long>(sm_count > 0 ? sm_count : 1) * 8;
@@ -73,14 +54,6 @@ cudaError_t launch_repack(const void *src, int64_t lds, void *dst, int64_t ldd, 
     else
         repack_rows_kernel<uint16_t><<<grid, 256, 0, stream>>>(
             static_cast<const uint16_t *>(src), lds, static_cast<uint16_t *>(dst), ldd, rows, cols);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_splitk_reduce(const float *partials, int splits, float *C, int64_t ldc,
-                                 int64_t M, int64_t N, int sm_count, cudaStream_t stream)
-{
-    if (M <= 0 || N <= 0) return cudaSuccess;
-    splitk_reduce_kernel<<<rows_grid(M, sm_count), 256, 0, stream>>>(partials, splits, C, ldc, M, N);
     return cudaGetLastError();
 }
 

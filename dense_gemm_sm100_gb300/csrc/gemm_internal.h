@@ -19,19 +19,30 @@ struct SimtTile {
     const char *name;
 };
 
-// Split of K into slices whose partial products are summed afterwards.
+// Split of K into slices for the tail of the tile order: the last
+// tail_tiles tiles (all of them for a uniform split) are each computed as
+// `splits` partial tiles that are summed afterwards.
 struct SplitK {
-    int splits = 1;           // 1 = write C directly
-    int k_per_split = 0;      // elements of K per slice (multiple of kSimtBK)
-    float *partials = nullptr;  // splits x M x N floats, row-major, when splits > 1
+    int splits = 1;             // 1 = no split: every tile writes C directly
+    int k_per_split = 0;        // elements of K per slice (multiple of kSimtBK)
+    int64_t tail_tiles = 0;     // tiles cut into slices
+    float *partials = nullptr;  // splits x tail_tiles tiles of bm x bn floats
 };
 
 int simt_num_configs();
 SimtTile simt_tile(int config, int layout_b);
-// Configuration for an M x N problem on a GPU with sm_count SMs.
-int simt_pick_config(int64_t M, int64_t N, int sm_count);
-// Number of K slices (and slice length) for an under-filled problem.
-SplitK simt_pick_splits(int config, int layout_b, int64_t M, int64_t N, int64_t K, int sm_count);
+// Configuration for an M x N x K problem on a GPU with sm_count SMs (grid
+// capped at max_ctas CTAs when max_ctas > 0).
+int simt_pick_config(int64_t M, int64_t N, int64_t K, int layout_b, int sm_count, int max_ctas);
+bool simt_config_usable(int config);  // false if the device cannot run it
+// K slices for the tiles of a partial last wave, on `slots` CTA slots.
+SplitK simt_pick_splits(int config, int layout_b, int64_t M, int64_t N, int64_t K, int64_t slots);
+// `want` slices (fewer if K is short) of the last `tail` of `tiles` tiles.
+SplitK simt_split_k(int64_t tiles, int64_t tail, int64_t want, int64_t K);
+// Work units of the persistent FP32 kernel, and the workspace its partial
+// tiles need.
+int64_t simt_units(int config, int layout_b, int64_t M, int64_t N, const SplitK &sk);
+size_t simt_partial_bytes(int config, int layout_b, const SplitK &sk);
 
 // Geometry of the tensor-core kernel (gemm_tc.cu).  A tile of C is
 // kTcBM x kTcBN; every stage holds 128 bytes of K per operand row, i.e.
@@ -60,11 +71,14 @@ cudaError_t prepare_tc();
 // FP32 SIMT GEMM with configuration `config`.  tmA maps A (dims {K, M}),
 // tmB maps the stored B (row-major: dims {N, K}; column-major: dims {K, N}),
 // both FP32 with a 128-byte swizzle and the boxes of simt_tile(config).
-// With sk.splits > 1 the kernel writes slice s of the product into
-// sk.partials + s*M*N (row-major, pitch N) and launch_splitk_reduce sums them.
+// With a split (sk.splits > 1) the kernel writes the tail tiles' slices to
+// sk.partials and launch_simt_tail_reduce, queued next with the same
+// arguments, sums them into C.
 cudaError_t launch_simt_f32(int config, const CUtensorMap &tmA, const CUtensorMap &tmB,
                             int layout_b, int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
                             const LaunchCommon &lc, const SplitK &sk = SplitK());
+cudaError_t launch_simt_tail_reduce(int config, int layout_b, int M, int N, int K, float *C, int64_t ldc,
+                                    bool c_vec4, const LaunchCommon &lc, const SplitK &sk, int sm_count);
 
 // Tensor-core GEMM; dtype is GEMM_TF32 or GEMM_BF16.  tmA/tmB as above.
 // tmC (may be null): C as FP32 dims {N, M}, box {32, 32}, 128-byte swizzle,
@@ -82,11 +96,6 @@ int tc_grid(int64_t M, int64_t N, int sm_count, int cluster);
 // dst[r*ldd + c] = src[r*lds + c] for r < rows, c < cols (elem_bytes 2 or 4).
 cudaError_t launch_repack(const void *src, int64_t lds, void *dst, int64_t ldd, int64_t rows,
                           int64_t cols, int elem_bytes, int sm_count, cudaStream_t stream);
-
-// C[i*ldc + j] = sum_{s < splits} partials[s*M*N + i*N + j], added in order
-// s = 0, 1, ... (deterministic).
-cudaError_t launch_splitk_reduce(const float *partials, int splits, float *C, int64_t ldc,
-                                 int64_t M, int64_t N, int sm_count, cudaStream_t stream);
 
 // C[i*ldc + j] = 0 for i < M, j < N.
 cudaError_t launch_zero_fill(float *C, int64_t ldc, int64_t M, int64_t N, int sm_count,

@@ -156,7 +156,7 @@ extern "C" int gemm_run_noalloc(int layout_b, int64_t M, int64_t N, int64_t K, c
     const bool c_vec4 = reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 4 == 0;
     cudaError_t e;
     if (dtype == GEMM_F32) {
-        const int cfg = dg::simt_pick_config(M, N, s->sm_count);
+        const int cfg = dg::simt_pick_config(M, N, K, layout_b, s->sm_count, 0);
         const dg::SimtTile t = dg::simt_tile(cfg, layout_b);
         bool ok = encode(&tmA, 4, A, K, M, lda_p, dg::kSimtBK, t.bm, CU_TENSOR_MAP_SWIZZLE_128B);
         ok = ok && (layout_b == GEMM_B_ROW_MAJOR

@@ -39,6 +39,21 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 }
 
 // Makes barrier initialisation visible to the async proxy (TMA, tcgen05).
+// Register reallocation between warpgroups: every warp of a warpgroup runs
+// the same instruction; the registers a CTA may hand out are those it was
+// launched with (threads x registers per thread at launch), which the host
+// checks before launching a kernel that raises its count.
+template <uint32_t R>
+__device__ __forceinline__ void setmaxnreg_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(R));
+}
+template <uint32_t R>
+__device__ __forceinline__ void setmaxnreg_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(R));
+}
+
 __device__ __forceinline__ void fence_barrier_init()
 {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

@@ -41,20 +41,24 @@ constexpr int BK = kSimtBK;  // 32 FP32 = one 128-byte swizzle row
 struct SimtParams {
     int M, N, K;
     int tiles_m, tiles_n, group_m;
-    int splits;          // K slices per tile (1 = no split)
-    int k_per_split;     // elements of K per slice, a multiple of BK
+    // Units [0, full_units) are whole tiles (tile order position = unit);
+    // then the last tail_tiles tiles of the order, each cut into `splits` K
+    // slices of k_per_split elements (a multiple of BK), whose partial tiles
+    // go to `partials` (slice-major, BM x BN floats each).
+    int full_units, tail_tiles, splits, k_per_split;
+    float *partials;
     float *C;
     long long ldc;
-    long long split_stride;  // elements between the partial-C slices
     int *status;
     unsigned long long timeout_ns;
     int c_vec4;
     int debug_drop;  // test hook: CTA 0 never loads its first stage
 };
 
-// Work unit u (persistent loop index) -> output tile and K slice.
+// Work unit u (persistent loop index) -> output tile and K range; split < 0
+// means the whole K range, written to C.
 struct Unit {
-    int mb, nb, kt_begin, kt_end, split;
+    int mb, nb, kt_begin, kt_end, split, slot;
 };
 
 // Tile t of the grouped order: groups of `group_m` tile rows, column-major
@@ -70,15 +74,27 @@ __device__ __forceinline__ void tile_coords(int t, const SimtParams &p, int &mb,
     nb = r / gm;
 }
 
-// Units run slice-major: unit u is tile u % tiles of K slice u / tiles.  The
-// K range of slice s is [s*k_per_split, min(K, (s+1)*k_per_split)) ("GEMM
-// 性能优化", 台阶 1: partial sums over K slices add up to the product).
+// Whole tiles first; the tail tiles run slice-major, so the slices of one
+// tile go to different CTAs of the last wave.  The K range of slice s is
+// [s*k_per_split, min(K, (s+1)*k_per_split)) ("GEMM 性能优化", 台阶 1:
+// partial sums over K slices add up to the product; Wave 模型: the last,
+// partial wave is spread over all CTAs).
 __device__ __forceinline__ Unit unit_coords(int u, const SimtParams &p)
 {
-    const int tiles = p.tiles_m * p.tiles_n;
     Unit w;
-    w.split = u / tiles;
-    tile_coords(u - w.split * tiles, p, w.mb, w.nb);
+    if (u < p.full_units) {
+        tile_coords(u, p, w.mb, w.nb);
+        w.kt_begin = 0;
+        w.kt_end = (p.K + kSimtBK - 1) / kSimtBK;
+        w.split = -1;
+        w.slot = 0;
+        return w;
+    }
+    const int v = u - p.full_units;
+    const int r = v % p.tail_tiles;
+    w.split = v / p.tail_tiles;
+    w.slot = v;  // = split * tail_tiles + r
+    tile_coords(p.full_units + r, p, w.mb, w.nb);
     const int k0 = w.split * p.k_per_split;
     const int k1 = min(p.K, k0 + p.k_per_split);
     w.kt_begin = k0 / kSimtBK;
@@ -99,7 +115,7 @@ __device__ __forceinline__ Unit unit_coords(int u, const SimtParams &p)
 // producer warp ("PMPP Chapter 06", section 1, corner turning): TMA lands the
 // K-contiguous tile, the warp rewrites it in the row-major staging layout,
 // and the consumers run the row-major (packed) inner loop.
-template <int LAYOUT_B, int WM, int WN, int TN, int STAGES, int GU, int F2>
+template <int LAYOUT_B, int WM, int WN, int TN, int STAGES, int GU, int F2, int PWG>
 struct Simt {
     static_assert(WM % 2 == 0, "row interleave pairs warps along M");
     static_assert(TN % 4 == 0 && TN <= 16, "thread tile width");
@@ -114,18 +130,29 @@ struct Simt {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + LAND_BYTES;
     static constexpr int NBAR = LAYOUT_B == 2 ? 3 : 2;  // full, empty (, ready)
     static constexpr int CONSUMER_WARPS = WM * WN;
-    static constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;
+    // PWG = 0: one producer warp, registers capped for all warps alike.
+    // PWG = 1: a producer warpgroup that gives up registers to the consumer
+    // warpgroups (setmaxnreg), so a thread can hold a wider tile of C.
+    static constexpr int PRODUCER_WARPS = PWG ? 4 : 1;
+    static constexpr int THREADS = (CONSUMER_WARPS + PRODUCER_WARPS) * 32;
+    static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8;  // what __launch_bounds__ allows
+    static constexpr int PRODUCER_REGS = CONSUMER_WARPS > 8 ? 24 : 40;
+    static constexpr int CONSUMER_REGS =
+        ((LAUNCH_REGS * THREADS - PRODUCER_REGS * PRODUCER_WARPS * 32) / (CONSUMER_WARPS * 32)) / 8 * 8 > 240
+            ? 240
+            : ((LAUNCH_REGS * THREADS - PRODUCER_REGS * PRODUCER_WARPS * 32) / (CONSUMER_WARPS * 32)) / 8 * 8;
+    static_assert(!PWG || (CONSUMER_WARPS % 4 == 0 && LAYOUT_B == 0), "warpgroups; row-major B only");
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NBAR * STAGES * 8 + 16;
     static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
     static_assert(BM <= 256 && BN <= 256, "TMA box limit");
 };
 
-template <int LAYOUT_B, int WM, int WN, int TN, int STAGES, int GU, int F2>
-__global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>::THREADS, 1)
+template <int LAYOUT_B, int WM, int WN, int TN, int STAGES, int GU, int F2, int PWG>
+__global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG>::THREADS, 1)
     sgemm_simt_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const SimtParams p)
 {
-    using S = Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>;
+    using S = Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG>;
     constexpr int BM = S::BM, BN = S::BN, A_BYTES = S::A_BYTES, STAGE_BYTES = S::STAGE_BYTES;
     constexpr int CONSUMER_WARPS = S::CONSUMER_WARPS;
 
@@ -144,7 +171,7 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>::TH
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int num_units = p.tiles_m * p.tiles_n * p.splits;
+    const int num_units = p.full_units + p.tail_tiles * p.splits;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -156,6 +183,15 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>::TH
         fence_barrier_init();
     }
     __syncthreads();
+
+    if (PWG) {
+        if (warp >= CONSUMER_WARPS) {
+            setmaxnreg_dec<S::PRODUCER_REGS>();
+            if (warp != CONSUMER_WARPS) return;  // one warp of the group issues the copies
+        } else {
+            setmaxnreg_inc<S::CONSUMER_REGS>();
+        }
+    }
 
     if (LAYOUT_B == 2 && warp == CONSUMER_WARPS) {
         // ------------------------------------------- producer + corner turn
@@ -404,15 +440,33 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>::TH
         }
 
         // ------------------------------------------------------ epilogue
-        // C itself, or the partial-sum slice of this unit's K range.
-        float *cbase = p.C + (long long)w.split * p.split_stride;
+        if (w.split >= 0) {
+            // A partial tile of a K slice: the whole BM x BN tile, rows and
+            // columns past M and N included (they hold zeros).
+            float *tile = p.partials + (long long)w.slot * (BM * BN);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float *trow = tile + (row0 + 8 * i) * BN;
+                if (RL == 0) {
+#pragma unroll
+                    for (int c = 0; c < TN / 4; ++c) {
+                        const float2 lo = acc2[i][2 * c], hi = acc2[i][2 * c + 1];
+                        *reinterpret_cast<float4 *>(trow + col0 + 32 * c) = make_float4(lo.x, lo.y, hi.x, hi.y);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < TN; ++j) trow[col0 + 8 * j] = (j & 1) ? acc2[i][j / 2].y : acc2[i][j / 2].x;
+                }
+            }
+            continue;
+        }
         const long long m_base = (long long)mb * BM + row0;
         const int n_base = nb * BN + col0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const long long m = m_base + 8 * i;
             if (m >= p.M) continue;
-            float *crow = cbase + m * p.ldc;
+            float *crow = p.C + m * p.ldc;
             if (RL == 0) {
                 // columns 32*c + {0..3}: pairs 2c and 2c + 1
 #pragma unroll
@@ -440,24 +494,72 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2>::TH
     }
 }
 
+// C for the tail tiles: the sum of their K-slice partial tiles, added in
+// slice order s = 0, 1, ... (deterministic; exact for integer data).  One
+// thread per 4 consecutive columns of a tile row.
+__global__ void __launch_bounds__(256) simt_tail_reduce_kernel(const SimtParams p, int bm, int bn)
+{
+    const int quads = bm * bn / 4;
+    const long long total = (long long)p.tail_tiles * quads;
+    const long long tile_elems = (long long)bm * bn;
+    for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < total;
+         q += (long long)gridDim.x * blockDim.x) {
+        const int r = static_cast<int>(q / quads);
+        const int e = static_cast<int>(q - (long long)r * quads) * 4;
+        const int row = e / bn, col = e - (e / bn) * bn;
+        int mb, nb;
+        tile_coords(p.full_units + r, p, mb, nb);
+        const long long m = (long long)mb * bm + row;
+        const int n = nb * bn + col;
+        if (m >= p.M || n >= p.N) continue;
+        const float *src = p.partials + (long long)r * tile_elems + e;
+        float4 acc = *reinterpret_cast<const float4 *>(src);
+        for (int s = 1; s < p.splits; ++s) {
+            const float4 v = *reinterpret_cast<const float4 *>(src + (long long)s * p.tail_tiles * tile_elems);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        float *c = p.C + m * p.ldc + n;
+        if (p.c_vec4 && n + 3 < p.N) {
+            *reinterpret_cast<float4 *>(c) = acc;
+        } else {
+            c[0] = acc.x;
+            if (n + 1 < p.N) c[1] = acc.y;
+            if (n + 2 < p.N) c[2] = acc.z;
+            if (n + 3 < p.N) c[3] = acc.w;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ configs
 
 struct ConfigEntry {
-    int bm, bn_row, bn_col, ctas_per_sm;
+    int bm, bn_row, bn_col, ctas_per_sm;  // ctas_per_sm 0: not usable on this device
+    float rate_row, rate_col;             // measured TFLOP/s in whole waves; 0: not picked automatically
     const char *name;
     cudaError_t (*prepare)(int *ctas_per_sm);
     void (*launch)(int layout_b, const CUtensorMap &, const CUtensorMap &, const SimtParams &,
                    int grid, cudaStream_t);
 };
 
-template <int L, int WM, int WN, int TN, int ST, int GU, int F2>
+template <int L, int WM, int WN, int TN, int ST, int GU, int F2, int PWG>
 cudaError_t prepare_one(int *ctas)
 {
-    using S = Simt<L, WM, WN, TN, ST, GU, F2>;
-    auto k = sgemm_simt_kernel<L, WM, WN, TN, ST, GU, F2>;
+    using S = Simt<L, WM, WN, TN, ST, GU, F2, PWG>;
+    auto k = sgemm_simt_kernel<L, WM, WN, TN, ST, GU, F2, PWG>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, k, S::THREADS, S::SMEM_BYTES);
+    if (e == cudaSuccess && PWG) {
+        // setmaxnreg.inc waits until the CTA's launch registers can cover the
+        // new counts; refuse the configuration unless they can.
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, k);
+        const int need = S::CONSUMER_REGS * S::CONSUMER_WARPS * 32 + S::PRODUCER_REGS * S::PRODUCER_WARPS * 32;
+        if (e == cudaSuccess && fa.numRegs * S::THREADS < need) *ctas = 0;
+    }
     return e;
 }
 
@@ -472,45 +574,53 @@ constexpr int col_stages(int wn, int tn, int f2, int st)
     return col_layout(wn, tn, f2) == 2 && st > 4 ? 4 : st;
 }
 
-template <int WM, int WN, int TN, int ST, int GU, int F2>
+// Column-major B always runs with one producer warp (its corner turn needs
+// the warp's registers).
+template <int WM, int WN, int TN, int ST, int GU, int F2, int PWG>
 cudaError_t prepare_cfg(int *ctas)
 {
     int c0 = 0, c1 = 0;
-    cudaError_t e = prepare_one<0, WM, WN, TN, ST, GU, F2>(&c0);
+    cudaError_t e = prepare_one<0, WM, WN, TN, ST, GU, F2, PWG>(&c0);
     if (e == cudaSuccess)
-        e = prepare_one<col_layout(WN, TN, F2), WM, WN, col_tn(TN), col_stages(WN, TN, F2, ST), GU, F2>(&c1);
+        e = prepare_one<col_layout(WN, TN, F2), WM, WN, col_tn(TN), col_stages(WN, TN, F2, ST), GU, F2, 0>(&c1);
     *ctas = c0 < c1 ? c0 : c1;
     return e;
 }
 
-template <int WM, int WN, int TN, int ST, int GU, int F2>
+template <int WM, int WN, int TN, int ST, int GU, int F2, int PWG>
 void launch_cfg(int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB, const SimtParams &p,
                 int grid, cudaStream_t stream)
 {
     if (layout_b == 0) {
-        using S = Simt<0, WM, WN, TN, ST, GU, F2>;
-        sgemm_simt_kernel<0, WM, WN, TN, ST, GU, F2><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
+        using S = Simt<0, WM, WN, TN, ST, GU, F2, PWG>;
+        sgemm_simt_kernel<0, WM, WN, TN, ST, GU, F2, PWG><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
     } else {
         constexpr int L = col_layout(WN, TN, F2), CST = col_stages(WN, TN, F2, ST);
-        using S = Simt<L, WM, WN, col_tn(TN), CST, GU, F2>;
-        sgemm_simt_kernel<L, WM, WN, col_tn(TN), CST, GU, F2><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
+        using S = Simt<L, WM, WN, col_tn(TN), CST, GU, F2, 0>;
+        sgemm_simt_kernel<L, WM, WN, col_tn(TN), CST, GU, F2, 0><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
     }
 }
 
-#define DG_SIMT_CFG(WM, WN, TN, ST, GU, F2, NAME)                                              \
-    {WM * 32, WN * 8 * TN, WN * 8 * col_tn(TN), 0, NAME, prepare_cfg<WM, WN, TN, ST, GU, F2>,  \
-     launch_cfg<WM, WN, TN, ST, GU, F2>}
+#define DG_SIMT_CFG(WM, WN, TN, ST, GU, F2, PWG, RATE_ROW, RATE_COL, NAME)                           \
+    {WM * 32,  WN * 8 * TN, WN * 8 * col_tn(TN), 0, RATE_ROW, RATE_COL, NAME,                          \
+     prepare_cfg<WM, WN, TN, ST, GU, F2, PWG>, launch_cfg<WM, WN, TN, ST, GU, F2, PWG>}
 
-// Config table; GEMM_OPT_SIMT_CONFIG selects entry (value - 1).
-// Measured at 8192^3 on GB300 (row-major B): 128x128 64.6 TFLOP/s, the same
-// tile with scalar FMAs 56.4, 64x128 59.2, 64x64 31.5; 8x16 per thread
-// (128x256) and 16 warps of 8x4 spill under the 168-register cap that the
-// producer warp's sub-partition sets, and run slower.
+// Config table; GEMM_OPT_SIMT_CONFIG selects entry (value - 1).  Rates are
+// TFLOP/s measured on GB300 at sizes that fill whole waves (M = 7296,
+// N = K = 8192); simt_pick_config weighs them against each shape's waves.
+// The scalar-FMA, 64x128 and 64x64 tiles (56.4, 59.2 and 31.5 at 8192^3),
+// 128x256 with register reallocation (8x16 per thread, 64.0) and 16
+// consumer warps of 8x4 (64.4) never win; they stay selectable.  12
+// consumer warps (3 per scheduler, 192x128) hide the multiply-add latency
+// better than 8 (67.3 against 64.9).
 ConfigEntry g_configs[] = {
-    DG_SIMT_CFG(4, 2, 8, 6, 8, 1, "128x128"),
-    DG_SIMT_CFG(4, 2, 8, 6, 8, 0, "128x128s"),
-    DG_SIMT_CFG(2, 2, 8, 4, 8, 1, "64x128"),
-    DG_SIMT_CFG(2, 1, 8, 4, 8, 1, "64x64"),
+    DG_SIMT_CFG(4, 2, 8, 6, 8, 1, 0, 64.9f, 60.0f, "128x128"),
+    DG_SIMT_CFG(4, 2, 8, 6, 8, 0, 0, 0.0f, 0.0f, "128x128s"),
+    DG_SIMT_CFG(2, 2, 8, 4, 8, 1, 0, 0.0f, 0.0f, "64x128"),
+    DG_SIMT_CFG(2, 1, 8, 4, 8, 1, 0, 0.0f, 0.0f, "64x64"),
+    DG_SIMT_CFG(4, 2, 16, 4, 8, 1, 1, 0.0f, 0.0f, "128x256r"),
+    DG_SIMT_CFG(6, 2, 8, 5, 8, 1, 1, 67.3f, 0.0f, "192x128r"),
+    DG_SIMT_CFG(4, 4, 4, 6, 8, 1, 1, 0.0f, 0.0f, "128x128w16"),
 };
 constexpr int kNumConfigs = sizeof(g_configs) / sizeof(g_configs[0]);
 
@@ -522,55 +632,101 @@ cudaError_t prepare_simt()
         int ctas = 0;
         cudaError_t e = g_configs[i].prepare(&ctas);
         if (e != cudaSuccess) return e;
-        g_configs[i].ctas_per_sm = ctas > 0 ? ctas : 1;
+        g_configs[i].ctas_per_sm = ctas;
     }
     return cudaSuccess;
 }
 
 int simt_num_configs() { return kNumConfigs; }
 
+bool simt_config_usable(int config)
+{
+    return config >= 0 && config < kNumConfigs && g_configs[config].ctas_per_sm > 0;
+}
+
 SimtTile simt_tile(int config, int layout_b)
 {
     const ConfigEntry &c = g_configs[config];
-    return SimtTile{c.bm, layout_b == 0 ? c.bn_row : c.bn_col, c.ctas_per_sm, c.name};
+    return SimtTile{c.bm, layout_b == 0 ? c.bn_row : c.bn_col, c.ctas_per_sm > 0 ? c.ctas_per_sm : 1, c.name};
 }
 
-int simt_pick_config(int64_t M, int64_t N, int sm_count)
-{
-    // The 128x128 tile everywhere: a smaller tile does not shorten a
-    // thread's serial chain of 64*K multiply-adds, which is what bounds an
-    // under-filled launch; split-K does (simt_pick_splits).
-    (void)M;
-    (void)N;
-    (void)sm_count;
-    return 0;
-}
+namespace {
 
-SplitK simt_pick_splits(int config, int layout_b, int64_t M, int64_t N, int64_t K, int sm_count)
+// Persistent waves a shape takes on `slots` CTA slots, counting a split
+// partial last wave as the fraction of a wave it lasts.
+double effective_waves(int config, int layout_b, int64_t M, int64_t N, int64_t K, int64_t slots)
 {
-    // Wave model ("GEMM 性能优化", Wave 模型): when the tiles fill less than one
-    // wave, cut K into slices so tiles x slices fill it, keeping at least
-    // four 32-element k-tiles per slice.
     const SimtTile t = simt_tile(config, layout_b);
     const int64_t tiles = ((M + t.bm - 1) / t.bm) * ((N + t.bn - 1) / t.bn);
-    const int64_t slots = int64_t{sm_count} * t.ctas_per_sm;
+    const SplitK sk = simt_pick_splits(config, layout_b, M, N, K, slots);
+    const int64_t tail = sk.splits > 1 ? sk.tail_tiles : 0;
+    const double last = tail > 0 ? 1.0 / sk.splits : 0.0;
+    return static_cast<double>((tiles - tail + slots - 1) / slots) + last;
+}
+
+}  // namespace
+
+int simt_pick_config(int64_t M, int64_t N, int64_t K, int layout_b, int sm_count, int max_ctas)
+{
+    // The configuration with the least estimated time: effective waves x
+    // tile area / measured rate ("GEMM 性能优化", Wave 模型).  A smaller tile
+    // does not shorten a thread's serial chain of multiply-adds, which is
+    // what bounds an under-filled launch; the K split does.
+    int best = 0;
+    double best_cost = -1.0;
+    for (int c = 0; c < kNumConfigs; ++c) {
+        const ConfigEntry &e = g_configs[c];
+        const float rate = layout_b == 0 ? e.rate_row : e.rate_col;
+        if (rate <= 0.0f || e.ctas_per_sm <= 0) continue;
+        const int64_t slots = max_ctas > 0 ? max_ctas : int64_t{sm_count} * e.ctas_per_sm;
+        const SimtTile t = simt_tile(c, layout_b);
+        const double cost = effective_waves(c, layout_b, M, N, K, slots) * t.bm * t.bn / rate;
+        if (best_cost < 0.0 || cost < best_cost) {
+            best_cost = cost;
+            best = c;
+        }
+    }
+    return best;
+}
+
+SplitK simt_pick_splits(int config, int layout_b, int64_t M, int64_t N, int64_t K, int64_t slots)
+{
+    // Wave model ("GEMM 性能优化", Wave 模型): the tiles that do not fill a
+    // whole wave (all of them when there are fewer tiles than slots) are cut
+    // into K slices so that tail x slices fills one wave, each slice at least
+    // four 32-element k-tiles long.
+    const SimtTile t = simt_tile(config, layout_b);
+    const int64_t tiles = ((M + t.bm - 1) / t.bm) * ((N + t.bn - 1) / t.bn);
     const int64_t k_tiles = (K + kSimtBK - 1) / kSimtBK;
-    int64_t s = tiles > 0 ? slots / tiles : 1;
+    SplitK sk;
+    if (tiles <= 0 || slots <= 0) return sk;
+    const int64_t tail = tiles < slots ? tiles : tiles % slots;
+    if (tail == 0) return sk;
+    int64_t s = slots / tail;
     s = s < k_tiles / 4 ? s : k_tiles / 4;
     s = s < 16 ? s : 16;
+    if (s <= 1) return sk;
+    return simt_split_k(tiles, tail, s, K);
+}
+
+SplitK simt_split_k(int64_t tiles, int64_t tail, int64_t want, int64_t K)
+{
     SplitK sk;
-    sk.splits = s > 1 ? static_cast<int>(s) : 1;
-    if (sk.splits > 1) {
-        const int64_t kt_per = (k_tiles + sk.splits - 1) / sk.splits;
-        sk.k_per_split = static_cast<int>(kt_per * kSimtBK);
-        sk.splits = static_cast<int>((k_tiles + kt_per - 1) / kt_per);  // no empty slice
-    }
+    const int64_t k_tiles = (K + kSimtBK - 1) / kSimtBK;
+    if (want > k_tiles) want = k_tiles;
+    if (want <= 1 || tail <= 0 || tail > tiles) return sk;
+    const int64_t kt_per = (k_tiles + want - 1) / want;
+    sk.splits = static_cast<int>((k_tiles + kt_per - 1) / kt_per);  // no empty slice
+    if (sk.splits <= 1) return SplitK();
+    sk.k_per_split = static_cast<int>(kt_per * kSimtBK);
+    sk.tail_tiles = tail;
     return sk;
 }
 
-cudaError_t launch_simt_f32(int config, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                            int layout_b, int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
-                            const LaunchCommon &lc, const SplitK &sk)
+namespace {
+
+SimtParams simt_params(int config, int layout_b, int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
+                       const LaunchCommon &lc, const SplitK &sk)
 {
     const SimtTile t = simt_tile(config, layout_b);
     SimtParams p;
@@ -580,16 +736,57 @@ cudaError_t launch_simt_f32(int config, const CUtensorMap &tmA, const CUtensorMa
     p.tiles_m = (M + t.bm - 1) / t.bm;
     p.tiles_n = (N + t.bn - 1) / t.bn;
     p.group_m = lc.group_m > 0 ? lc.group_m : 8;
-    p.splits = sk.splits > 1 ? sk.splits : 1;
-    p.k_per_split = p.splits > 1 ? sk.k_per_split : K;
-    p.C = p.splits > 1 ? sk.partials : C;
-    p.ldc = p.splits > 1 ? N : ldc;
-    p.split_stride = static_cast<long long>(M) * N;
+    const bool split = sk.splits > 1 && sk.tail_tiles > 0;
+    p.tail_tiles = split ? static_cast<int>(sk.tail_tiles) : 0;
+    p.splits = split ? sk.splits : 1;
+    p.k_per_split = split ? sk.k_per_split : K;
+    p.full_units = p.tiles_m * p.tiles_n - p.tail_tiles;
+    p.partials = split ? sk.partials : nullptr;
+    p.C = C;
+    p.ldc = ldc;
     p.status = lc.status;
     p.timeout_ns = lc.timeout_ns;
-    p.c_vec4 = p.splits > 1 ? (N % 4 == 0) : (c_vec4 ? 1 : 0);
+    p.c_vec4 = c_vec4 ? 1 : 0;
     p.debug_drop = lc.debug_drop;
+    return p;
+}
+
+}  // namespace
+
+int64_t simt_units(int config, int layout_b, int64_t M, int64_t N, const SplitK &sk)
+{
+    const SimtTile t = simt_tile(config, layout_b);
+    const int64_t tiles = ((M + t.bm - 1) / t.bm) * ((N + t.bn - 1) / t.bn);
+    return sk.splits > 1 && sk.tail_tiles > 0 ? tiles - sk.tail_tiles + sk.tail_tiles * sk.splits : tiles;
+}
+
+size_t simt_partial_bytes(int config, int layout_b, const SplitK &sk)
+{
+    const SimtTile t = simt_tile(config, layout_b);
+    if (sk.splits <= 1 || sk.tail_tiles <= 0) return 0;
+    return static_cast<size_t>(sk.splits) * static_cast<size_t>(sk.tail_tiles) * t.bm * t.bn * sizeof(float);
+}
+
+cudaError_t launch_simt_f32(int config, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                            int layout_b, int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
+                            const LaunchCommon &lc, const SplitK &sk)
+{
+    const SimtParams p = simt_params(config, layout_b, M, N, K, C, ldc, c_vec4, lc, sk);
     g_configs[config].launch(layout_b, tmA, tmB, p, lc.grid, lc.stream);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_simt_tail_reduce(int config, int layout_b, int M, int N, int K, float *C, int64_t ldc,
+                                    bool c_vec4, const LaunchCommon &lc, const SplitK &sk, int sm_count)
+{
+    const SimtParams p = simt_params(config, layout_b, M, N, K, C, ldc, c_vec4, lc, sk);
+    if (p.tail_tiles == 0) return cudaSuccess;
+    const SimtTile t = simt_tile(config, layout_b);
+    const long long threads = (long long)p.tail_tiles * (t.bm * t.bn / 4);
+    long long blocks = (threads + 255) / 256;
+    const long long cap = 8LL * (sm_count > 0 ? sm_count : 1);
+    if (blocks > cap) blocks = cap;
+    simt_tail_reduce_kernel<<<static_cast<int>(blocks), 256, 0, lc.stream>>>(p, t.bm, t.bn);
     return cudaGetLastError();
 }
 

@@ -69,6 +69,9 @@ WORKLOADS = {
 # still larger than L2 (129 MB) but a few hundred MB in total.
 PROFILE_WORKLOADS = {
     "fp32_4096_row": Workload("fp32_4096_row", 4096, 4096, 4096, B_ROW_MAJOR, "uniform", 3),
+    # 19 x 32 tiles of 192 x 128 = 4 whole waves on 152 SMs; A, B, C 184 MiB
+    "fp32_3648x4096x4096_row": Workload("fp32_3648x4096x4096_row", 3648, 4096, 4096, B_ROW_MAJOR,
+                                        "uniform", 3),
     "ffn_bf16_4096x7168x4096": Workload("ffn_bf16_4096x7168x4096", 4096, 7168, 4096,
                                         B_ROW_MAJOR, "normal", 4, 0.02, BF16),
     "ffn_tf32_4096x7168x4096": Workload("ffn_tf32_4096x7168x4096", 4096, 7168, 4096,

@@ -81,7 +81,7 @@ extern "C" {
 #define GEMM_OPT_SIMT_GROUP_M 3   /* tile-order group height in tiles for the FP32 kernel */
 #define GEMM_OPT_TC_GROUP_M 4     /* tile-order group height in tiles for the tensor-core kernel */
 #define GEMM_OPT_MAX_CTAS 5       /* cap on persistent CTAs (0 = SMs x resident CTAs per SM) */
-#define GEMM_OPT_SIMT_CONFIG 6    /* FP32 tile configuration: 0 = chosen per shape, else 1..4 */
+#define GEMM_OPT_SIMT_CONFIG 6    /* FP32 tile configuration: 0 = chosen per shape, else 1..5 */
 #define GEMM_OPT_SPLIT_K 7        /* FP32 K slices: 0 = chosen per shape, 1 = none, 2..64 = forced */
 #define GEMM_OPT_TC_CLUSTER 8     /* tensor-core mode: 1 one CTA per tile, 2 CTA pairs sharing B by multicast, 3 pair MMA (cta_group::2, default) */
 #define GEMM_OPT_TC_TMA_STORE 9   /* 1 (default): tensor-core epilogue stores C by TMA when aligned */

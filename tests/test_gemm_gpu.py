@@ -241,67 +241,81 @@ def test_run_host_matches_device(g, mode, layout):
     assert torch.equal(Cd, Ch)
 
 
-@pytest.mark.parametrize("mode,layout,max_ctas,shape,blocks", [
-    ("f32", ROW, 2, (2048, 2048, 256), "2x2"),    # row panels x column panels of B
-    ("f32", COL, 4, (3000, 3000, 256), "6x1"),    # ragged last row panel, all columns
-    ("f32", ROW, 2, (3000, 1000, 256), "2x1"),    # a 440-row rest would be cut along K: joined
-    ("f32", ROW, 2, (10000, 256, 1024), "2x1"),   # panels grow to 4992 rows, none cut along K
-    ("f32", COL, 4, (2000, 1000, 512), "1x1"),    # copies outweigh the compute: one block
-    ("bf16", ROW, 16, (1000, 3000, 256), "1x2"),  # one row panel in two column blocks
+HOST_BLOCK_CASES = [  # mode, layout, CTA cap, shape, blocks (None: one launch)
+    ("f32", ROW, 2, (2048, 2048, 256), None),
+    ("f32", COL, 4, (3000, 3000, 256), "12x1"),
+    ("f32", ROW, 2, (3000, 1000, 256), None),
+    ("f32", ROW, 2, (10000, 256, 1024), "14x1"),
+    ("f32", COL, 4, (2000, 1000, 512), None),
+    ("bf16", ROW, 16, (1000, 3000, 256), "1x2"),
     ("bf16", COL, 8, (1000, 3000, 256), "2x2"),
-    ("bf16", ROW, 8, (3000, 3000, 1024), "6x2"),  # pair MMA blocks
+    ("bf16", ROW, 8, (3000, 3000, 1024), "6x2"),
     ("tf32", COL, 8, (2300, 2000, 512), "5x2"),
     ("tf32", ROW, 4, (1000, 1000, 512), "2x2"),
-])
-def test_run_host_blocks_match_device(g, mode, layout, max_ctas, shape, blocks):
+]
+
+
+@pytest.mark.parametrize("mode,layout,max_ctas,shape,blocks", HOST_BLOCK_CASES)
+def test_run_host_blocks_match_oracle(g, oracle_mod, mode, layout, max_ctas, shape, blocks):
     """gemm_run_host cuts C into blocks (row panels of A x column panels of B)
-    whose copies in and out overlap the GEMMs of the neighbouring blocks; the
-    result is bit-identical to one device-resident call, also with host
-    leading dimensions wider than the matrix.  The tile-slot cap shrinks the
-    blocks so that small problems exercise the plan."""
+    whose copies in and out overlap the GEMMs of the neighbouring blocks.  The
+    tile-slot cap shrinks the waves so that small problems exercise the
+    plans; host leading dimensions are wider than the matrices.  Same
+    tolerance as one call, exact on integer inputs, nothing written past N."""
     from dense_gemm_sm100_gb300 import gemm
     M, N, K = shape
     g.set_option(gemm.GEMM_OPT_MAX_CTAS, max_ctas)
     try:
-        A, B = inp.make_operands(M, N, K, layout_b=layout, seed=M + N, dtype=mode)
-        Cd = run_gpu(g, A, B, layout, mode).cpu()
-        Ap = torch.zeros((M, K + 5), dtype=A.dtype).pin_memory()[:, :K]
-        Ap.copy_(A)
-        Bp = torch.zeros((B.shape[0], B.shape[1] + 7), dtype=B.dtype).pin_memory()[:, :B.shape[1]]
-        Bp.copy_(B)
-        Ch = torch.full((M, N + 3), -1.0).pin_memory()
-        g.run_host(Ap, Bp, Ch[:, :N], layout, mode)
-        g.sync_status()
-        assert g.last_path.startswith("host+")
-        assert ("+blocks" not in g.last_path) if blocks == "1x1" else g.last_path.endswith(f"+blocks{blocks}")
-        assert torch.equal(Cd, Ch[:, :N])
-        assert torch.all(Ch[:, N:] == -1.0)  # nothing written past N
+        for integer in (False, True):
+            if integer:
+                A, B = inp.make_integer_operands(M, N, K, layout_b=layout, seed=M, dtype=mode)
+            else:
+                A, B = inp.make_operands(M, N, K, layout_b=layout, dist="normal", seed=M + N, dtype=mode)
+            Ap = torch.zeros((M, K + 5), dtype=A.dtype).pin_memory()[:, :K]
+            Ap.copy_(A)
+            Bp = torch.zeros((B.shape[0], B.shape[1] + 7), dtype=B.dtype).pin_memory()[:, :B.shape[1]]
+            Bp.copy_(B)
+            Ch = torch.full((M, N + 3), -1.0).pin_memory()
+            g.run_host(Ap, Bp, Ch[:, :N], layout, mode)
+            g.sync_status()
+            torch.cuda.synchronize()
+            assert g.last_path.startswith("host+")
+            if blocks is None:
+                assert "+blocks" not in g.last_path
+            else:
+                assert g.last_path.endswith(f"+blocks{blocks}"), g.last_path
+            assert torch.all(Ch[:, N:] == -1.0)  # nothing written past N
+            Cr, S = oracle_of(oracle_mod, A, B, layout)
+            if integer:
+                assert np.array_equal(to_f64(Ch[:, :N]), Cr), g.last_path
+            else:
+                assert_parity(Ch[:, :N], Cr, S, TOL[mode], g.last_path)
     finally:
         g.set_option(gemm.GEMM_OPT_MAX_CTAS, 0)
 
 
-def test_run_host_orders_with_the_callers_stream(g):
+def test_run_host_orders_with_the_callers_stream(g, oracle_mod):
     """The copies of A and B start after work queued earlier on the caller's
     stream (here: the copy that fills the host buffer of A), and C is
     complete once that stream is synchronised."""
     from dense_gemm_sm100_gb300 import gemm
-    g.set_option(gemm.GEMM_OPT_MAX_CTAS, 2)
+    g.set_option(gemm.GEMM_OPT_MAX_CTAS, 4)
     try:
         s = torch.cuda.Stream()
-        M, N, K = 2048, 2048, 256
-        A, B = inp.make_operands(M, N, K, seed=7)
+        M, N, K = 3000, 3000, 256
+        A, B = inp.make_integer_operands(M, N, K, layout_b=COL, seed=7)
         A_d = A.cuda()
-        Cd = run_gpu(g, A, B, ROW, "f32").cpu()
+        Cr, _ = oracle_of(oracle_mod, A, B, COL)
         for _ in range(3):
             Ap = torch.zeros((M, K)).pin_memory()
             Ch = torch.zeros((M, N)).pin_memory()
             with torch.cuda.stream(s):
                 torch.cuda._sleep(2_000_000)  # keep the stream busy before the fill
                 Ap.copy_(A_d, non_blocking=True)
-            g.run_host(Ap, B.pin_memory(), Ch, ROW, "f32", stream=s)
+            g.run_host(Ap, B.pin_memory(), Ch, COL, "f32", stream=s)
             s.synchronize()
-            assert g.last_path.endswith("+blocks2x2")
-            assert torch.equal(Cd, Ch)
+            assert g.last_path.endswith("+blocks12x1")
+            assert np.array_equal(to_f64(Ch), Cr)
     finally:
         g.set_option(gemm.GEMM_OPT_MAX_CTAS, 0)
 
@@ -347,6 +361,32 @@ def test_cluster_pairs_match_oracle_and_single_cta(g, oracle_mod, cluster_mode, 
 
 # ------------------------------------------------------- split-K (FP32 path)
 
+SIMT_CONFIG_SHAPES = [(1, 1, 1), (129, 257, 33), (300, 520, 260), (640, 1030, 512)]
+
+
+@pytest.mark.parametrize("config", [1, 2, 3, 4, 5, 6, 7])
+@pytest.mark.parametrize("layout", [ROW, COL])
+@pytest.mark.parametrize("shape", SIMT_CONFIG_SHAPES)
+def test_simt_configs_match_oracle(g, oracle_mod, config, layout, shape):
+    """Every FP32 tile configuration (GEMM_OPT_SIMT_CONFIG 1..5: 128x128
+    packed and scalar, 64x128, 64x64, and 128x256 with register reallocation
+    for row-major B) on ragged shapes spanning several tiles."""
+    from dense_gemm_sm100_gb300 import gemm
+    M, N, K = shape
+    g.set_option(gemm.GEMM_OPT_SIMT_CONFIG, config)
+    try:
+        A, B = inp.make_operands(M, N, K, layout_b=layout, dist="normal", seed=M + N + K + config)
+        C = run_gpu(g, A, B, layout, "f32")
+        Cr, S = oracle_mod.gemm(to_f64(A), to_f64(B), layout)
+        assert_parity(C, Cr, S, TOL["f32"], f"config {config} {shape}")
+        Ai, Bi = inp.make_integer_operands(M, N, K, layout_b=layout, seed=config)
+        Ci = run_gpu(g, Ai, Bi, layout, "f32")
+        Cri, _ = oracle_mod.gemm(to_f64(Ai), to_f64(Bi), layout)
+        assert np.array_equal(to_f64(Ci), Cri), f"config {config} integer inputs"
+    finally:
+        g.set_option(gemm.GEMM_OPT_SIMT_CONFIG, 0)
+
+
 @pytest.mark.parametrize("layout", [ROW, COL])
 @pytest.mark.parametrize("splits", [2, 3, 7])
 def test_split_k_forced(g, oracle_mod, layout, splits):
@@ -385,6 +425,35 @@ def test_split_k_chosen_for_underfilled_shape(g):
     A, B = inp.make_operands(1024, 1024, 1024, layout_b=COL, seed=1)
     run_gpu(g, A, B, COL, "f32")
     assert "splitk" in g.last_path
+
+
+@pytest.mark.parametrize("config,layout,M", [(1, ROW, 700), (1, COL, 700), (6, ROW, 500)])
+def test_tail_tiles_split_along_k(g, oracle_mod, config, layout, M):
+    """Tiles of a partial last wave are cut into K slices spread over all CTA
+    slots, and a second kernel adds the slices in order ("GEMM 性能优化",
+    Wave 模型).  An 8-CTA cap makes the wave small: 700 rows x 650 columns
+    in 128x128 tiles is 36 tiles = 4 waves + 4 tiles, 500 rows in 192x128
+    tiles is 18 tiles = 2 waves + 2 tiles.  Same tolerance, deterministic,
+    and exact on integer inputs."""
+    from dense_gemm_sm100_gb300 import gemm
+    N, K = 650, 640
+    g.set_option(gemm.GEMM_OPT_MAX_CTAS, 8)
+    g.set_option(gemm.GEMM_OPT_SIMT_CONFIG, config)
+    try:
+        A, B = inp.make_operands(M, N, K, layout_b=layout, dist="normal", seed=M + config)
+        C1 = run_gpu(g, A, B, layout, "f32").cpu()
+        assert "+tail" in g.last_path, g.last_path
+        C2 = run_gpu(g, A, B, layout, "f32").cpu()
+        Ai, Bi = inp.make_integer_operands(M, N, K, layout_b=layout, seed=config)
+        Ci = run_gpu(g, Ai, Bi, layout, "f32")
+    finally:
+        g.set_option(gemm.GEMM_OPT_MAX_CTAS, 0)
+        g.set_option(gemm.GEMM_OPT_SIMT_CONFIG, 0)
+    assert torch.equal(C1, C2)
+    Cr, S = oracle_of(oracle_mod, A, B, layout)
+    assert_parity(C1, Cr, S, TOL["f32"], f"tail split config {config}")
+    Cri, _ = oracle_of(oracle_mod, Ai, Bi, layout)
+    assert np.array_equal(to_f64(Ci), Cri)
 
 
 # ------------------------------------------------------- the five workloads
