@@ -46,6 +46,7 @@ NOMINAL_PF = {"bf16": 2.25, "tf32": 1.1}
 # ncu capture of the kernel as it is now; None until captured for this version.
 # Key: workload name -> (bytes per launch, summary file under profiles/).
 NCU_TRAFFIC: dict[str, tuple[float, str]] = {
+    "fp32_8192_row": (2713.7e6 + 255.9e6, "profiles/dram_traffic_full_size.md"),
 }
 
 DESCRIPTIONS = {
@@ -177,6 +178,19 @@ def time_device(run, stream, steps, warmup, counter=None):
     return starts[0].elapsed_time(ends[-1]), per, c1 - c0
 
 
+L2_BYTES = 129e6
+
+
+def l2_note(res) -> str:
+    """How the timed steps relate to the L2 cache (no flush between steps)."""
+    es = 2 if res["dtype"] == "bf16" else 4
+    total = es * (res["M"] * res["K"] + res["K"] * res["N"]) + 4 * res["M"] * res["N"]
+    mib = total / 2**20
+    if total > L2_BYTES:
+        return f"inputs larger than L2 (A, B, C {mib:.0f} MiB vs 129 MB L2); no flush"
+    return f"A, B, C ({mib:.1f} MiB) fit in the 129 MB L2: warm-L2 steps, no flush"
+
+
 def bench_workload(g, name, steps, warmup, dist_ctx, peaks, peak_note, with_e2e, side_cublas=False):
     import torch
     from dense_gemm_sm100_gb300 import inputs as inp
@@ -217,7 +231,8 @@ def bench_workload(g, name, steps, warmup, dist_ctx, peaks, peak_note, with_e2e,
         "workload": name, "description": DESCRIPTIONS.get(name, name),
         "M": w.M, "N": w.N, "K": w.K, "layout_b": "row" if w.layout_b == 0 else "col",
         "dtype": w.dtype, "value": value, "ms_per_step": ms_max, "kernel_ms": kernel_ms,
-        "kernel_ms_min": min(per), "path": g.last_path, "roofline": roof,
+        "kernel_ms_min": min(per), "kernel_ms_median": statistics.median(per),
+        "path": g.last_path, "roofline": roof,
         "launches_timed": launches, "wall_window": (t0, t1),
         "compulsory_bytes": rl.compulsory_bytes(w.M, w.N, w.K, es),
     }
@@ -503,10 +518,12 @@ def main(argv=None):
         "dtype": main_res["dtype"], "data": "synthetic",
         "config": {"workload": main_res["description"], "M": main_res["M"], "N": main_res["N"],
                    "K": main_res["K"], "layout_b": main_res["layout_b"], "path": main_res["path"],
-                   "l2": "inputs larger than L2 (A, B, C 768 MiB vs 129 MB L2); no flush",
+                   "l2": l2_note(main_res),
                    "parallelism": f"replicas{n}" if n > 1 else "single-gpu"},
         "roofline": main_res["roofline"],
         "kernel_ms": main_res["kernel_ms"],
+        "kernel_ms_median": main_res["kernel_ms_median"],
+        "kernel_ms_min": main_res["kernel_ms_min"],
         "gpu_launches": main_res["launches_timed"],
         "clocks": clocks,
         "e2e": e2e,
