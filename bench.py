@@ -87,6 +87,28 @@ def roofline_entry(bound, achieved, peak, unit, traffic, note):
             "traffic": traffic, "peak_source": note}
 
 
+def measure_peaks():
+    """The compute roofs measured on this GPU by the library's own
+    microbenchmarks (include/gemm_peaks.h), each launch ~20-50 ms, best of 3."""
+    from dense_gemm_sm100_gb300 import gemm
+    out = {}
+    for kind, iters in (("ffma", 320000), ("ffma2", 320000), ("mma_bf16", 64000), ("mma_tf32", 64000)):
+        r = gemm.measure_peak(kind, iters)
+        out[f"{kind}_tflops"] = round(r["tflops"], 2)
+    out["what"] = ("FP32 multiply-adds on the CUDA cores, scalar and packed pairs (32 warps/SM of "
+                   "independent chains); tcgen05 MMA 128x256 from shared memory into tensor memory, "
+                   "one CTA per SM, no copies")
+    return out
+
+
+def add_microbench(roof, peak):
+    """Beside the contract's peak: the same kernel against the microbenchmark roof."""
+    if roof is None or not peak:
+        return
+    roof["peak_microbench"] = peak
+    roof["frac_of_microbench"] = round(roof["achieved"] / peak, 4)
+
+
 def aggregate(ms_per_rank, flops_per_rank_step):
     """Whole-job throughput over ranks: total work / slowest rank's time."""
     ms = max(ms_per_rank)
@@ -434,6 +456,8 @@ def main(argv=None):
     ap.add_argument("--no-modes", action="store_true", help="skip the tensor-core workloads")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-peaks", action="store_true",
+                    help="skip the FMA and tensor-core peak microbenchmarks")
     ap.add_argument("--no-side-reference", action="store_true",
                     help="skip the labelled cuBLAS side reference")
     ap.add_argument("--ladder", action="store_true",
@@ -474,6 +498,11 @@ def main(argv=None):
     if sampler:
         sampler.stop()
         clocks = sampler.summary(*main_res["wall_window"])
+    measured = None
+    if not args.no_peaks:
+        measured = measure_peaks()
+        if measured:
+            add_microbench(main_res["roofline"], measured.get("ffma2_tflops"))
     modes = []
     if not args.no_modes:
         for name in TC_WORKLOADS:
@@ -484,6 +513,8 @@ def main(argv=None):
                                with_e2e=False, side_cublas=not args.no_side_reference)
             m = {k: r[k] for k in ("workload", "description", "dtype", "value",
                                    "ms_per_step", "kernel_ms", "path", "roofline")}
+            if measured:
+                add_microbench(m["roofline"], measured.get(f"mma_{r['dtype']}_tflops"))
             if "cublas_side" in r:
                 m["cublas_side"] = r["cublas_side"]
             if msampler:
@@ -530,6 +561,7 @@ def main(argv=None):
         "cpu_baseline": cpu,
         "modes": modes,
         "cublas_side": side.get(args.workload),
+        "peaks_measured": measured,
     }
     print(json.dumps(line))
     return 0

@@ -4,9 +4,10 @@ The functions ``gemm_create``, ``gemm_run``, ``gemm_run_host``,
 ``gemm_destroy``, ``gemm_validate``, ``gemm_sync_status``,
 ``gemm_set_option``, ``gemm_last_error_string``, ``gemm_status_string``,
 ``gemm_last_path``, ``gemm_launch_count``, ``gemm_version``,
-``gemm_run_noalloc``, ``gemm_ladder_run`` and ``gemm_ladder_name`` take and
-return
-the same plain values as their C counterparts (pointers as ints).  ``Gemm``
+``gemm_run_noalloc``, ``gemm_ladder_run``, ``gemm_ladder_name``,
+``gemm_peak_fma_run`` and ``gemm_peak_mma_run`` take and return the same
+plain values as their C counterparts (pointers as ints; the FLOP-count
+out-parameter of the peak calls is returned as a second value).  ``Gemm``
 wraps a handle for torch tensors.  Every GEMM step runs in the library's CUDA
 kernels; there is no other code path, and calling anything here without the
 built library raises ``GemmLibraryMissing``.
@@ -93,6 +94,8 @@ def load_library():
             "gemm_run_noalloc": ([ci, i64, i64, i64, vp, i64, vp, i64, vp, i64, ci, vp], ci),
             "gemm_ladder_run": ([ci, i64, i64, i64, vp, vp, vp, vp], ci),
             "gemm_ladder_name": ([ci], ctypes.c_char_p),
+            "gemm_peak_fma_run": ([ci, i64, vp, vp, ctypes.POINTER(ctypes.c_double)], ci),
+            "gemm_peak_mma_run": ([ci, i64, vp, ctypes.c_uint64, vp, ctypes.POINTER(ctypes.c_double)], ci),
         }
         for name, (argtypes, restype) in sig.items():
             fn = getattr(lib, name)
@@ -181,6 +184,55 @@ def gemm_ladder_run(step, M, N, K, A, B, C, stream) -> int:
 
 def gemm_ladder_name(step) -> str:
     return load_library().gemm_ladder_name(step).decode()
+
+
+# Peak-rate microbenchmarks (include/gemm_peaks.h): the compute roofs.
+
+def gemm_peak_fma_run(packed, iters, sink, stream) -> tuple[int, float]:
+    flops = ctypes.c_double(0.0)
+    rc = load_library().gemm_peak_fma_run(packed, iters, sink, stream, ctypes.byref(flops))
+    return rc, flops.value
+
+
+def gemm_peak_mma_run(dtype, iters, status, timeout_ns, stream) -> tuple[int, float]:
+    flops = ctypes.c_double(0.0)
+    rc = load_library().gemm_peak_mma_run(dtype, iters, status, timeout_ns, stream, ctypes.byref(flops))
+    return rc, flops.value
+
+
+def measure_peak(kind: str, iters: int, reps: int = 3, stream=None) -> dict:
+    """Time the microbenchmark `kind` ("ffma", "ffma2", "mma_bf16",
+    "mma_tf32") with CUDA events on `stream`: one warm-up launch, then the
+    best of `reps` launches.  Returns TFLOP/s and the launch time."""
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    sh = _stream_handle(s)
+    sink = torch.zeros(2, dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def launch():
+        if kind in ("ffma", "ffma2"):
+            rc, fl = gemm_peak_fma_run(1 if kind == "ffma2" else 0, iters, sink.data_ptr(), sh)
+        else:
+            dt = GEMM_BF16 if kind == "mma_bf16" else GEMM_TF32
+            rc, fl = gemm_peak_mma_run(dt, iters, status.data_ptr(), 0, sh)
+        if rc != GEMM_OK:
+            raise GemmError(rc, f"{kind} microbenchmark: {gemm_status_string(rc)}")
+        return fl
+
+    launch()
+    best_ms, flops = None, 0.0
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        flops = launch()
+        e1.record(s)
+        e1.synchronize()
+        ms = e0.elapsed_time(e1)
+        best_ms = ms if best_ms is None else min(best_ms, ms)
+    if int(status.item()) != 0:
+        raise GemmError(GEMM_ERR_TIMEOUT, f"{kind} microbenchmark: a wait expired")
+    return {"tflops": flops / (best_ms * 1e-3) / 1e12, "ms": best_ms, "flops": flops}
 
 
 # ------------------------------------------------------------- torch wrapper

@@ -9,7 +9,8 @@ import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gemm.h")
-HEADERS = [HEADER, os.path.join(ROOT, "include", "gemm_ladder.h")]
+HEADERS = [HEADER, os.path.join(ROOT, "include", "gemm_ladder.h"),
+           os.path.join(ROOT, "include", "gemm_peaks.h")]
 
 
 @pytest.fixture(scope="module")
@@ -31,7 +32,7 @@ def test_header_declares_the_abi():
     names = declared_functions()
     for required in ("gemm_create", "gemm_run", "gemm_destroy", "gemm_run_host",
                      "gemm_validate", "gemm_sync_status", "gemm_last_error_string",
-                     "gemm_run_noalloc", "gemm_ladder_run"):
+                     "gemm_run_noalloc", "gemm_ladder_run", "gemm_peak_fma_run", "gemm_peak_mma_run"):
         assert required in names
 
 
@@ -100,6 +101,17 @@ def test_ladder_rejects_bad_shapes_without_gpu(lib):
     assert g.gemm_ladder_run(1, 0, 4, 4, P, P, P, None) == g.GEMM_ERR_INVALID
     assert g.gemm_ladder_name(2).startswith("2 shared-memory tiling")
     assert g.gemm_ladder_name(77) == ""
+
+
+def test_peak_microbenchmarks_reject_bad_arguments_without_gpu(lib):
+    from dense_gemm_sm100_gb300 import gemm as g
+    # argument checks happen before any device call
+    assert g.gemm_peak_fma_run(2, 16, P, None)[0] == g.GEMM_ERR_INVALID    # packed not 0/1
+    assert g.gemm_peak_fma_run(1, 17, P, None)[0] == g.GEMM_ERR_INVALID    # iters % 16
+    assert g.gemm_peak_fma_run(1, 0, P, None)[0] == g.GEMM_ERR_INVALID
+    assert g.gemm_peak_fma_run(0, 16, 0, None)[0] == g.GEMM_ERR_INVALID    # no sink
+    assert g.gemm_peak_mma_run(g.GEMM_F32, 10, 0, 0, None)[0] == g.GEMM_ERR_INVALID
+    assert g.gemm_peak_mma_run(g.GEMM_BF16, 0, 0, 0, None)[0] == g.GEMM_ERR_INVALID
 
 
 def test_null_handle_calls_are_rejected(lib):
