@@ -365,6 +365,70 @@ PAGES_LADDER_PCT = {1: (6, 11), 2: (25, 40), 3: (50, 65), 4: (60, 75), 5: (70, 8
                     6: (80, 87), 7: (90, 97)}
 
 
+def run_configs(args):
+    """Every workload of the specification, timed two ways: warm (back-to-back
+    steps) and with the L2 scrubbed before each step (a 2 x L2 buffer written
+    between the event pairs, outside the timed region), median and min of the
+    per-step CUDA-event times; then the oracle on the two small cases with one
+    host thread and with all of them.  One JSON document."""
+    import torch
+    import oracle
+    from dense_gemm_sm100_gb300 import gemm
+    from dense_gemm_sm100_gb300 import inputs as inp
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    steps = max(5, min(args.steps, 30))
+    scrub = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
+    g = gemm.Gemm(0)
+    out = []
+    for name, w in inp.WORKLOADS.items():
+        A, B = inp.make_workload(w)
+        A_d, B_d = A.to(dev), B.to(dev)
+        C_d = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
+
+        def run():
+            g.run(A_d, B_d, C_d, w.layout_b, w.dtype, stream)
+
+        _, warm, _ = time_device(run, stream, steps, args.warmup)
+        path = g.last_path
+        for _ in range(args.warmup):
+            run()
+        cold = []
+        for _ in range(steps):
+            scrub.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run()
+            e1.record(stream)
+            e1.synchronize()
+            cold.append(e0.elapsed_time(e1))
+        g.sync_status(stream)
+        tf = lambda ms: round(w.flops / (ms * 1e-3) / 1e12, 3)
+        out.append({"workload": name, "description": DESCRIPTIONS.get(name, name), "dtype": w.dtype,
+                    "path": path, "steps": steps,
+                    "warm": {"ms_median": statistics.median(warm), "ms_min": min(warm),
+                             "tflops_median": tf(statistics.median(warm)), "tflops_max": tf(min(warm))},
+                    "l2_scrubbed": {"ms_median": statistics.median(cold), "ms_min": min(cold),
+                                    "tflops_median": tf(statistics.median(cold)),
+                                    "tflops_max": tf(min(cold))}})
+        del A_d, B_d, C_d
+        torch.cuda.empty_cache()
+    g.close()
+    cpu = []
+    for name in ("fp32_128_row", "fp32_1024_colB"):
+        w = inp.WORKLOADS[name]
+        A, B = inp.make_workload(w)
+        A64, B64 = A.double().numpy(), B.double().numpy()
+        for threads in (1, oracle.default_threads()):
+            t = time.perf_counter()
+            oracle.gemm(A64, B64, w.layout_b, nthreads=threads)
+            dt = time.perf_counter() - t
+            cpu.append({"workload": name, "threads": threads, "seconds": round(dt, 4),
+                        "gflops": round(w.flops / dt / 1e9, 3)})
+    print(json.dumps({"configs": out, "oracle": cpu}))
+    return 0
+
+
 def run_ladder(args):
     """Time every kernel of the labelled ladder suite (include/gemm_ladder.h),
     this library's FP32 path and cuBLAS SGEMM (TF32 off) on one square
@@ -462,6 +526,9 @@ def main(argv=None):
                     help="skip the labelled cuBLAS side reference")
     ap.add_argument("--ladder", action="store_true",
                     help="time the labelled ladder suite (pages' optimisation steps) instead")
+    ap.add_argument("--configs", action="store_true",
+                    help="time every specified workload warm and with L2 scrubbed, and the oracle "
+                         "on the small ones with 1 and all host threads (one JSON document)")
     ap.add_argument("--ladder-size", type=int, default=4096)
     ap.add_argument("--ladder-steps", default="1,2,3,4,5,6,7,8,101,102")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -475,6 +542,8 @@ def main(argv=None):
         return run_reference(args, ctx)
     if args.ladder:
         return run_ladder(args)
+    if args.configs:
+        return run_configs(args)
 
     import torch
     from dense_gemm_sm100_gb300 import gemm
