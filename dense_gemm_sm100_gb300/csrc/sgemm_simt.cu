@@ -142,6 +142,9 @@ struct Simt {
             ? 240
             : ((LAUNCH_REGS * THREADS - PRODUCER_REGS * PRODUCER_WARPS * 32) / (CONSUMER_WARPS * 32)) / 8 * 8;
     static_assert(!PWG || (CONSUMER_WARPS % 4 == 0 && LAYOUT_B == 0), "warpgroups; row-major B only");
+    // 16 consumer warps leave 112 registers a thread: A fragments are then
+    // loaded 2 k at a time (8-byte loads) instead of 4, to fit.
+    static constexpr bool A_PAIRS = CONSUMER_WARPS >= 16;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NBAR * STAGES * 8 + 16;
     static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
     static_assert(BM <= 256 && BN <= 256, "TMA box limit");
@@ -387,9 +390,12 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
                 for (int h = 0; h < GU; ++h) {
                     const int g = g0 + h;
                     const uint8_t *ap = st + a_base + ((g ^ xa) << 4);
-                    float4 a[8];
+                    float4 a[S::A_PAIRS ? 1 : 8];
+                    float2 a2[S::A_PAIRS ? 8 : 1];
+                    if (!S::A_PAIRS) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) a[i] = *reinterpret_cast<const float4 *>(ap + i * 1024);
+                        for (int i = 0; i < 8; ++i) a[i] = *reinterpret_cast<const float4 *>(ap + i * 1024);
+                    }
                     float4 bcol[RL == 0 ? 1 : TN];
                     if (RL != 0) {
                         const uint8_t *bp = st + b_base + ((g ^ lc) << 4);
@@ -398,6 +404,11 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
                     }
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
+                        if (S::A_PAIRS && (kk & 1) == 0) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                a2[i] = *reinterpret_cast<const float2 *>(ap + i * 1024 + (kk >> 1) * 8);
+                        }
                         // b2[jp] = columns (2*jp, 2*jp + 1) of B row k = 4*g + kk.
                         float2 b2[TN / 2];
                         if (RL == 0) {
@@ -419,7 +430,8 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
                         }
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
-                            const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+                            const float av = S::A_PAIRS ? ((kk & 1) ? a2[i].y : a2[i].x)
+                                             : kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
                             if (F2 && RL == 0) {
                                 const float2 aa = make_float2(av, av);
 #pragma unroll
@@ -569,9 +581,13 @@ cudaError_t prepare_one(int *ctas)
 // (layout 1).
 constexpr int col_tn(int tn) { return tn < 8 ? tn : 8; }
 constexpr int col_layout(int wn, int tn, int f2) { return (f2 && wn * 8 * col_tn(tn) == 128) ? 2 : 1; }
-constexpr int col_stages(int wn, int tn, int f2, int st)
+constexpr int col_stages(int wm, int wn, int tn, int f2, int st)
 {
-    return col_layout(wn, tn, f2) == 2 && st > 4 ? 4 : st;
+    // at most 4 stages, and as many of A + B + landing zone as fit in 227 KB
+    return col_layout(wn, tn, f2) != 2 ? st
+           : (st < 4 ? st : 4) < (232448 - 2048) / (wm * 32 * 128 + 2 * wn * 8 * col_tn(tn) * 128)
+               ? (st < 4 ? st : 4)
+               : (232448 - 2048) / (wm * 32 * 128 + 2 * wn * 8 * col_tn(tn) * 128);
 }
 
 // Column-major B always runs with one producer warp (its corner turn needs
@@ -582,7 +598,7 @@ cudaError_t prepare_cfg(int *ctas)
     int c0 = 0, c1 = 0;
     cudaError_t e = prepare_one<0, WM, WN, TN, ST, GU, F2, PWG>(&c0);
     if (e == cudaSuccess)
-        e = prepare_one<col_layout(WN, TN, F2), WM, WN, col_tn(TN), col_stages(WN, TN, F2, ST), GU, F2, 0>(&c1);
+        e = prepare_one<col_layout(WN, TN, F2), WM, WN, col_tn(TN), col_stages(WM, WN, TN, F2, ST), GU, F2, 0>(&c1);
     *ctas = c0 < c1 ? c0 : c1;
     return e;
 }
@@ -595,7 +611,7 @@ void launch_cfg(int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB, co
         using S = Simt<0, WM, WN, TN, ST, GU, F2, PWG>;
         sgemm_simt_kernel<0, WM, WN, TN, ST, GU, F2, PWG><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
     } else {
-        constexpr int L = col_layout(WN, TN, F2), CST = col_stages(WN, TN, F2, ST);
+        constexpr int L = col_layout(WN, TN, F2), CST = col_stages(WM, WN, TN, F2, ST);
         using S = Simt<L, WM, WN, col_tn(TN), CST, GU, F2, 0>;
         sgemm_simt_kernel<L, WM, WN, col_tn(TN), CST, GU, F2, 0><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
     }
@@ -606,21 +622,24 @@ void launch_cfg(int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB, co
      prepare_cfg<WM, WN, TN, ST, GU, F2, PWG>, launch_cfg<WM, WN, TN, ST, GU, F2, PWG>}
 
 // Config table; GEMM_OPT_SIMT_CONFIG selects entry (value - 1).  Rates are
-// TFLOP/s measured on GB300 at sizes that fill whole waves (M = 7296,
-// N = K = 8192); simt_pick_config weighs them against each shape's waves.
-// The scalar-FMA, 64x128 and 64x64 tiles (56.4, 59.2 and 31.5 at 8192^3),
-// 128x256 with register reallocation (8x16 per thread, 64.0) and 16
-// consumer warps of 8x4 (64.4) never win; they stay selectable.  12
-// consumer warps (3 per scheduler, 192x128) hide the multiply-add latency
-// better than 8 (67.3 against 64.9).
+// TFLOP/s measured on GB300 at sizes that fill whole waves (M = 7296 or
+// 14592, N = 8192); simt_pick_config weighs them against each shape's
+// waves.  The scalar-FMA, 64x128 and 64x64 tiles (56.4, 59.2 and 31.5 at
+// 8192^3), 128x256 with register reallocation (8x16 per thread, 64.0), 16
+// consumer warps of 8x4 (64.4) and 16 consumer warps of 8x8 with A loaded
+// in pairs (256x128, 112 registers, spills: 59.3) never win; they stay
+// selectable.  12 consumer warps (3 per scheduler, 192x128) hide the
+// multiply-add latency better than 8 (67.4 against 64.4); with scalar FMAs
+// instead of packed pairs the same tile is issue-bound (57.7).
 ConfigEntry g_configs[] = {
     DG_SIMT_CFG(4, 2, 8, 6, 8, 1, 0, 64.9f, 60.0f, "128x128"),
     DG_SIMT_CFG(4, 2, 8, 6, 8, 0, 0, 0.0f, 0.0f, "128x128s"),
     DG_SIMT_CFG(2, 2, 8, 4, 8, 1, 0, 0.0f, 0.0f, "64x128"),
     DG_SIMT_CFG(2, 1, 8, 4, 8, 1, 0, 0.0f, 0.0f, "64x64"),
     DG_SIMT_CFG(4, 2, 16, 4, 8, 1, 1, 0.0f, 0.0f, "128x256r"),
-    DG_SIMT_CFG(6, 2, 8, 5, 8, 1, 1, 67.3f, 0.0f, "192x128r"),
+    DG_SIMT_CFG(6, 2, 8, 4, 8, 1, 1, 67.3f, 0.0f, "192x128r"),
     DG_SIMT_CFG(4, 4, 4, 6, 8, 1, 1, 0.0f, 0.0f, "128x128w16"),
+    DG_SIMT_CFG(8, 2, 8, 4, 8, 1, 1, 0.0f, 0.0f, "256x128r"),
 };
 constexpr int kNumConfigs = sizeof(g_configs) / sizeof(g_configs[0]);
 
@@ -628,10 +647,16 @@ constexpr int kNumConfigs = sizeof(g_configs) / sizeof(g_configs[0]);
 
 cudaError_t prepare_simt()
 {
+    // A configuration the device cannot run is marked unusable (never picked,
+    // refused by GEMM_OPT_SIMT_CONFIG); only the default one must work.
     for (int i = 0; i < kNumConfigs; ++i) {
         int ctas = 0;
         cudaError_t e = g_configs[i].prepare(&ctas);
-        if (e != cudaSuccess) return e;
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            if (i == 0) return e;
+            ctas = 0;
+        }
         g_configs[i].ctas_per_sm = ctas;
     }
     return cudaSuccess;

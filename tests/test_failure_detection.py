@@ -19,18 +19,19 @@ from tests._parity import TOL, assert_parity, to_f64
 
 pytestmark = pytest.mark.gpu
 
-CASES = [
-    ("f32", inp.B_ROW_MAJOR, None),
-    ("f32", inp.B_COL_MAJOR, None),
-    ("bf16", inp.B_ROW_MAJOR, 1),
-    ("bf16", inp.B_ROW_MAJOR, 2),
-    ("bf16", inp.B_COL_MAJOR, 3),
-    ("tf32", inp.B_ROW_MAJOR, 3),
+CASES = [  # mode, layout, tensor-core mode, FP32 configuration (0 = chosen)
+    ("f32", inp.B_ROW_MAJOR, None, 0),
+    ("f32", inp.B_COL_MAJOR, None, 0),
+    ("f32", inp.B_ROW_MAJOR, None, 6),  # producer warpgroup with register reallocation
+    ("bf16", inp.B_ROW_MAJOR, 1, 0),
+    ("bf16", inp.B_ROW_MAJOR, 2, 0),
+    ("bf16", inp.B_COL_MAJOR, 3, 0),
+    ("tf32", inp.B_ROW_MAJOR, 3, 0),
 ]
 
 
-@pytest.mark.parametrize("mode,layout,tc_mode", CASES)
-def test_expired_wait_is_reported_and_context_survives(oracle_mod, mode, layout, tc_mode):
+@pytest.mark.parametrize("mode,layout,tc_mode,simt_config", CASES)
+def test_expired_wait_is_reported_and_context_survives(oracle_mod, mode, layout, tc_mode, simt_config):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from dense_gemm_sm100_gb300 import build, gemm
@@ -44,6 +45,7 @@ def test_expired_wait_is_reported_and_context_survives(oracle_mod, mode, layout,
         g.set_option(gemm.GEMM_OPT_WAIT_TIMEOUT_NS, 20_000_000)  # 20 ms
         if tc_mode is not None:
             g.set_option(gemm.GEMM_OPT_TC_CLUSTER, tc_mode)
+        g.set_option(gemm.GEMM_OPT_SIMT_CONFIG, simt_config)
         g.sync_status()  # clean start
 
         g.set_option(gemm.GEMM_OPT_DEBUG_DROP_LOAD, 1)

@@ -294,6 +294,26 @@ def test_run_host_blocks_match_oracle(g, oracle_mod, mode, layout, max_ctas, sha
         g.set_option(gemm.GEMM_OPT_MAX_CTAS, 0)
 
 
+@pytest.mark.parametrize("mode", MODES)
+def test_run_host_pageable_memory(g, oracle_mod, mode):
+    """Host buffers that are not page-locked work too (the copies then block
+    the calling thread); large enough to be cut into blocks."""
+    from dense_gemm_sm100_gb300 import gemm
+    g.set_option(gemm.GEMM_OPT_MAX_CTAS, 8)
+    try:
+        M, N, K = 3000, 3000, 1024
+        A, B = inp.make_integer_operands(M, N, K, seed=11, dtype=mode)
+        C = torch.full((M, N), -1.0)
+        g.run_host(A, B, C, ROW, mode)
+        g.sync_status()
+        torch.cuda.synchronize()
+        assert "+blocks" in g.last_path, g.last_path
+    finally:
+        g.set_option(gemm.GEMM_OPT_MAX_CTAS, 0)
+    Cr, _ = oracle_of(oracle_mod, A, B, ROW)
+    assert np.array_equal(to_f64(C), Cr)
+
+
 def test_run_host_orders_with_the_callers_stream(g, oracle_mod):
     """The copies of A and B start after work queued earlier on the caller's
     stream (here: the copy that fills the host buffer of A), and C is
@@ -364,7 +384,7 @@ def test_cluster_pairs_match_oracle_and_single_cta(g, oracle_mod, cluster_mode, 
 SIMT_CONFIG_SHAPES = [(1, 1, 1), (129, 257, 33), (300, 520, 260), (640, 1030, 512)]
 
 
-@pytest.mark.parametrize("config", [1, 2, 3, 4, 5, 6, 7])
+@pytest.mark.parametrize("config", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("layout", [ROW, COL])
 @pytest.mark.parametrize("shape", SIMT_CONFIG_SHAPES)
 def test_simt_configs_match_oracle(g, oracle_mod, config, layout, shape):
