@@ -47,6 +47,8 @@ NOMINAL_PF = {"bf16": 2.25, "tf32": 1.1}
 # Key: workload name -> (bytes per launch, summary file under profiles/).
 NCU_TRAFFIC: dict[str, tuple[float, str]] = {
     "fp32_8192_row": (2713.7e6 + 255.9e6, "profiles/dram_traffic_full_size.md"),
+    "ffn_bf16_8192x14336x4096": (600.4e6 + 432.8e6, "profiles/dram_traffic_full_size.md"),
+    "ffn_tf32_8192x14336x4096": (1820.8e6 + 447.1e6, "profiles/dram_traffic_full_size.md"),
 }
 
 DESCRIPTIONS = {
@@ -567,6 +569,10 @@ def main(argv=None):
     if sampler:
         sampler.stop()
         clocks = sampler.summary(*main_res["wall_window"])
+        if clocks and clocks.get("sm_mhz"):
+            f = clocks["sm_mhz"] / peaks["sm_max_mhz"]
+            r = main_res["roofline"]
+            r["frac_at_observed_clock"] = round(r["achieved"] / (r["peak"] * f), 4) if f > 0 else None
     measured = None
     if not args.no_peaks:
         measured = measure_peaks()
