@@ -405,6 +405,11 @@ def run_configs(args):
             e1.synchronize()
             cold.append(e0.elapsed_time(e1))
         g.sync_status(stream)
+        # labelled side reference: cuBLAS through torch on the same operands
+        torch.backends.cuda.matmul.allow_tf32 = w.dtype == "tf32"
+        Bl = B_d if w.layout_b == 0 else B_d.t()
+        _, cub, _ = time_device(lambda: torch.matmul(A_d, Bl), stream, steps, args.warmup)
+        torch.backends.cuda.matmul.allow_tf32 = False
         tf = lambda ms: round(w.flops / (ms * 1e-3) / 1e12, 3)
         out.append({"workload": name, "description": DESCRIPTIONS.get(name, name), "dtype": w.dtype,
                     "path": path, "steps": steps,
@@ -412,7 +417,11 @@ def run_configs(args):
                              "tflops_median": tf(statistics.median(warm)), "tflops_max": tf(min(warm))},
                     "l2_scrubbed": {"ms_median": statistics.median(cold), "ms_min": min(cold),
                                     "tflops_median": tf(statistics.median(cold)),
-                                    "tflops_max": tf(min(cold))}})
+                                    "tflops_max": tf(min(cold))},
+                    "cublas_side": {"tflops_median": tf(statistics.median(cub)),
+                                    "what": "torch.matmul (cuBLAS), warm, " +
+                                            ("BF16 output" if w.dtype == "bf16" else
+                                             "TF32 allowed" if w.dtype == "tf32" else "TF32 off")}})
         del A_d, B_d, C_d
         torch.cuda.empty_cache()
     g.close()
