@@ -81,8 +81,17 @@ extern "C" {
 #define GEMM_OPT_SIMT_GROUP_M 3   /* tile-order group height in tiles for the FP32 kernel */
 #define GEMM_OPT_TC_GROUP_M 4     /* tile-order group height in tiles for the tensor-core kernel */
 #define GEMM_OPT_MAX_CTAS 5       /* cap on persistent CTAs (0 = SMs x resident CTAs per SM) */
-#define GEMM_OPT_SIMT_CONFIG 6    /* FP32 tile configuration: 0 = chosen per shape, else 1..5 */
-#define GEMM_OPT_SPLIT_K 7        /* FP32 K slices: 0 = chosen per shape, 1 = none, 2..64 = forced */
+/* FP32 tile configuration: 0 = chosen per shape (least estimated time), else
+ * 1..8 = 128x128, 128x128 scalar FMA, 64x128, 64x64, 128x256 (8x16 per
+ * thread), 192x128 (12 consumer warps, the usual row-major choice), 128x128
+ * with 16 consumer warps, 256x128 with 16 consumer warps.  A configuration
+ * the device cannot run is refused with GEMM_ERR_INVALID. */
+#define GEMM_OPT_SIMT_CONFIG 6
+/* FP32 K slices.  0 = chosen per shape: the tiles of a partial last wave
+ * (all tiles when they fill less than one wave) are cut into K slices that
+ * a second kernel adds in slice order.  1 = never.  2..64 = every tile cut
+ * into that many slices (fewer if K is short). */
+#define GEMM_OPT_SPLIT_K 7
 #define GEMM_OPT_TC_CLUSTER 8     /* tensor-core mode: 1 one CTA per tile, 2 CTA pairs sharing B by multicast, 3 pair MMA (cta_group::2, default) */
 #define GEMM_OPT_TC_TMA_STORE 9   /* 1 (default): tensor-core epilogue stores C by TMA when aligned */
 /* Test hook for failure detection, 0 by default.  1: in the next runs, CTA 0
