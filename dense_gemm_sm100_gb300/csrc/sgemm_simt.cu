@@ -136,12 +136,13 @@ struct Simt {
     static constexpr int PRODUCER_WARPS = PWG ? 4 : 1;
     static constexpr int THREADS = (CONSUMER_WARPS + PRODUCER_WARPS) * 32;
     static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8;  // what __launch_bounds__ allows
-    static constexpr int PRODUCER_REGS = CONSUMER_WARPS > 8 ? 24 : 40;
+    // the corner turn (column-major B) needs a few more registers than the copies alone
+    static constexpr int PRODUCER_REGS = CONSUMER_WARPS > 8 ? (LAYOUT_B == 2 ? 32 : 24) : 40;
     static constexpr int CONSUMER_REGS =
         ((LAUNCH_REGS * THREADS - PRODUCER_REGS * PRODUCER_WARPS * 32) / (CONSUMER_WARPS * 32)) / 8 * 8 > 240
             ? 240
             : ((LAUNCH_REGS * THREADS - PRODUCER_REGS * PRODUCER_WARPS * 32) / (CONSUMER_WARPS * 32)) / 8 * 8;
-    static_assert(!PWG || (CONSUMER_WARPS % 4 == 0 && LAYOUT_B == 0), "warpgroups; row-major B only");
+    static_assert(!PWG || (CONSUMER_WARPS % 4 == 0 && LAYOUT_B != 1), "warpgroups; B read as row-major");
     // 16 consumer warps leave 112 registers a thread: A fragments are then
     // loaded 2 k at a time (8-byte loads) instead of 4, to fit.
     static constexpr bool A_PAIRS = CONSUMER_WARPS >= 16;
@@ -180,7 +181,7 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar + 8 * s, 1);
             mbar_init(empty_bar + 8 * s, CONSUMER_WARPS);
-            if (LAYOUT_B == 2) mbar_init(ready_bar + 8 * s, 1);
+            if (LAYOUT_B == 2) mbar_init(ready_bar + 8 * s, S::PRODUCER_WARPS);  // every turning warp
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -190,21 +191,28 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
     if (PWG) {
         if (warp >= CONSUMER_WARPS) {
             setmaxnreg_dec<S::PRODUCER_REGS>();
-            if (warp != CONSUMER_WARPS) return;  // one warp of the group issues the copies
+            // one warp of the group issues the copies; with column-major B
+            // all four share the corner turn
+            if (warp != CONSUMER_WARPS && LAYOUT_B != 2) return;
         } else {
             setmaxnreg_inc<S::CONSUMER_REGS>();
         }
     }
 
-    if (LAYOUT_B == 2 && warp == CONSUMER_WARPS) {
+    if (LAYOUT_B == 2 && warp >= CONSUMER_WARPS) {
         // ------------------------------------------- producer + corner turn
-        // Lane 0 keeps the ring STAGES-1 k-tiles ahead; all lanes turn each
-        // landed K-major B tile (rows n, 128 bytes of k) into the row-major
-        // staging layout (4 boxes of 32 k-rows x 32 columns, 128-byte
-        // swizzle) that the consumers read.  Lane (g, t) = (lane/8, lane%8)
-        // moves 4x4 blocks of rows 4*(8g+t)..+3 and k-chunk t ^ r (r < 8):
-        // inside each group of 8 lanes both the 16-byte reads and the 16-byte
-        // writes land on 8 distinct bank groups.
+        // Lane 0 of the first producer warp keeps the ring STAGES-1 k-tiles
+        // ahead; the producer warps turn each landed K-major B tile (rows n,
+        // 128 bytes of k) into the row-major staging layout (4 boxes of 32
+        // k-rows x 32 columns, 128-byte swizzle) that the consumers read.
+        // Lane (g, t) = (lane/8, lane%8) moves 4x4 blocks of rows
+        // 4*(8g+t)..+3 and k-chunk t ^ r: inside each group of 8 lanes both
+        // the 16-byte reads and the 16-byte writes land on 8 distinct bank
+        // groups.  With P producer warps, warp w turns r = w*8/P .. +8/P-1;
+        // each arrives on the stage's ready barrier (count P) when done.
+        constexpr int R_PER = 8 / S::PRODUCER_WARPS;
+        const int pw = warp - CONSUMER_WARPS;
+        const bool issuer = pw == 0;
         uint32_t issued = 0;
         int iss_unit = blockIdx.x, iss_kt = 0, iss_kt_end = 0, iss_mb = 0, iss_nb = 0;
         auto iss_load_unit = [&]() {
@@ -238,7 +246,7 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
             return true;
         };
         bool ok = true;
-        if (lane == 0) {
+        if (issuer && lane == 0) {
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
             iss_load_unit();
@@ -264,7 +272,8 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
                 const uint8_t *land = smem + s * STAGE_BYTES + LAND;
                 uint8_t *brow = smem + s * STAGE_BYTES + A_BYTES + tg * 4096;
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
+                for (int rr = 0; rr < R_PER; ++rr) {
+                    const int r = pw * R_PER + rr;
                     const int c = tt ^ r;  // k chunk: k = 4c .. 4c + 3
                     float4 v[4];
 #pragma unroll
@@ -285,12 +294,12 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(ready_bar + 8 * s);
-                    if (iss_unit < num_units) ok = issue_next();
+                    if (issuer && iss_unit < num_units) ok = issue_next();
                 }
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             }
         }
-        if (!ok && lane == 0) {
+        if (!ok && issuer && lane == 0) {
             // Leave no copy in flight: wait (bounded) for every stage issued
             // but not yet turned.
             for (uint32_t i = it; i < issued; ++i) {
@@ -590,15 +599,19 @@ constexpr int col_stages(int wm, int wn, int tn, int f2, int st)
                : (232448 - 2048) / (wm * 32 * 128 + 2 * wn * 8 * col_tn(tn) * 128);
 }
 
-// Column-major B always runs with one producer warp (its corner turn needs
-// the warp's registers).
+// Column-major B uses the producer warpgroup only when it is turned in
+// shared memory (layout 2); the transposed-read kernel (layout 1) keeps one
+// producer warp.
+constexpr int col_pwg(int wn, int tn, int f2, int pwg) { return pwg && col_layout(wn, tn, f2) == 2 ? 1 : 0; }
+
 template <int WM, int WN, int TN, int ST, int GU, int F2, int PWG>
 cudaError_t prepare_cfg(int *ctas)
 {
     int c0 = 0, c1 = 0;
     cudaError_t e = prepare_one<0, WM, WN, TN, ST, GU, F2, PWG>(&c0);
     if (e == cudaSuccess)
-        e = prepare_one<col_layout(WN, TN, F2), WM, WN, col_tn(TN), col_stages(WM, WN, TN, F2, ST), GU, F2, 0>(&c1);
+        e = prepare_one<col_layout(WN, TN, F2), WM, WN, col_tn(TN), col_stages(WM, WN, TN, F2, ST), GU, F2,
+                        col_pwg(WN, TN, F2, PWG)>(&c1);
     *ctas = c0 < c1 ? c0 : c1;
     return e;
 }
@@ -612,8 +625,9 @@ void launch_cfg(int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB, co
         sgemm_simt_kernel<0, WM, WN, TN, ST, GU, F2, PWG><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
     } else {
         constexpr int L = col_layout(WN, TN, F2), CST = col_stages(WM, WN, TN, F2, ST);
-        using S = Simt<L, WM, WN, col_tn(TN), CST, GU, F2, 0>;
-        sgemm_simt_kernel<L, WM, WN, col_tn(TN), CST, GU, F2, 0><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
+        constexpr int CP = col_pwg(WN, TN, F2, PWG);
+        using S = Simt<L, WM, WN, col_tn(TN), CST, GU, F2, CP>;
+        sgemm_simt_kernel<L, WM, WN, col_tn(TN), CST, GU, F2, CP><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
     }
 }
 
@@ -629,15 +643,17 @@ void launch_cfg(int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB, co
 // consumer warps of 8x4 (64.4) and 16 consumer warps of 8x8 with A loaded
 // in pairs (256x128, 112 registers, spills: 59.3) never win; they stay
 // selectable.  12 consumer warps (3 per scheduler, 192x128) hide the
-// multiply-add latency better than 8 (67.4 against 64.4); with scalar FMAs
-// instead of packed pairs the same tile is issue-bound (57.7).
+// multiply-add latency better than 8 (67.4 against 64.4; column-major B,
+// its corner turn shared by the four producer warps, 62.3 against 60.0);
+// with scalar FMAs instead of packed pairs the same tile is issue-bound
+// (57.7).
 ConfigEntry g_configs[] = {
     DG_SIMT_CFG(4, 2, 8, 6, 8, 1, 0, 64.9f, 60.0f, "128x128"),
     DG_SIMT_CFG(4, 2, 8, 6, 8, 0, 0, 0.0f, 0.0f, "128x128s"),
     DG_SIMT_CFG(2, 2, 8, 4, 8, 1, 0, 0.0f, 0.0f, "64x128"),
     DG_SIMT_CFG(2, 1, 8, 4, 8, 1, 0, 0.0f, 0.0f, "64x64"),
     DG_SIMT_CFG(4, 2, 16, 4, 8, 1, 1, 0.0f, 0.0f, "128x256r"),
-    DG_SIMT_CFG(6, 2, 8, 4, 8, 1, 1, 67.3f, 0.0f, "192x128r"),
+    DG_SIMT_CFG(6, 2, 8, 4, 8, 1, 1, 67.3f, 62.3f, "192x128r"),
     DG_SIMT_CFG(4, 4, 4, 6, 8, 1, 1, 0.0f, 0.0f, "128x128w16"),
     DG_SIMT_CFG(8, 2, 8, 4, 8, 1, 1, 0.0f, 0.0f, "256x128r"),
 };

@@ -243,7 +243,7 @@ def test_run_host_matches_device(g, mode, layout):
 
 HOST_BLOCK_CASES = [  # mode, layout, CTA cap, shape, blocks (None: one launch)
     ("f32", ROW, 2, (2048, 2048, 256), None),
-    ("f32", COL, 4, (3000, 3000, 256), "12x1"),
+    ("f32", COL, 4, (3000, 3000, 256), "16x1"),
     ("f32", ROW, 2, (3000, 1000, 256), None),
     ("f32", ROW, 2, (10000, 256, 1024), "14x1"),
     ("f32", COL, 4, (2000, 1000, 512), None),
@@ -334,7 +334,7 @@ def test_run_host_orders_with_the_callers_stream(g, oracle_mod):
                 Ap.copy_(A_d, non_blocking=True)
             g.run_host(Ap, B.pin_memory(), Ch, COL, "f32", stream=s)
             s.synchronize()
-            assert g.last_path.endswith("+blocks12x1")
+            assert g.last_path.endswith("+blocks16x1")
             assert np.array_equal(to_f64(Ch), Cr)
     finally:
         g.set_option(gemm.GEMM_OPT_MAX_CTAS, 0)
