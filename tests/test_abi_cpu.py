@@ -122,6 +122,30 @@ def test_null_handle_calls_are_rejected(lib):
     assert g.gemm_launch_count(None) == 0
 
 
+C_CHECK = os.path.join(ROOT, "tests", "c_abi", "gemm_abi_check.c")
+
+
+def c_abi_build_cmd(out, cuda_home):
+    return ["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+            "-isystem", os.path.join(cuda_home, "include"), C_CHECK,
+            "-L", os.path.join(ROOT, "dense_gemm_sm100_gb300"), "-ldense_gemm_gb300",
+            "-L", os.path.join(cuda_home, "lib64"), "-lcudart",
+            "-Wl,-rpath," + os.path.join(ROOT, "dense_gemm_sm100_gb300"), "-o", out]
+
+
+def test_headers_are_plain_c_and_the_library_links(lib, tmp_path):
+    """The three public headers compile as C99 with warnings as errors, and a
+    C program links against the library (run on the GPU by
+    tests/test_c_abi_gpu.py)."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no gcc")
+    cuda_home = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    r = subprocess.run(c_abi_build_cmd(str(tmp_path / "abi_check"), cuda_home), capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     from dense_gemm_sm100_gb300 import gemm as g
     monkeypatch.setattr(g, "LIB_PATH", str(tmp_path / "absent.so"))
