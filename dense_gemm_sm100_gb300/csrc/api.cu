@@ -201,6 +201,31 @@ int encode_2d(gemm_ctx *h, CUtensorMap *map, int es, const void *base, int64_t i
     return GEMM_OK;
 }
 
+// Row-major B as a 3-D tensor of 128-byte column chunks: {column in chunk,
+// k, chunk}, strides ld*es and chunk*es bytes.  Only for N a multiple of the
+// chunk, so no box reaches past the last row of B.
+int encode_b_chunks(gemm_ctx *h, CUtensorMap *map, int es, const void *base, int64_t N, int64_t K, int64_t ld,
+                    int box_k, int box_chunks, CUtensorMapSwizzle swizzle)
+{
+    const int64_t chunk = 128 / es;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(chunk), static_cast<cuuint64_t>(K),
+                                static_cast<cuuint64_t>(N / chunk)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * es, static_cast<cuuint64_t>(chunk) * es};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(chunk), static_cast<cuuint32_t>(box_k),
+                               static_cast<cuuint32_t>(box_chunks)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt = es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const CUresult r = g_encode(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char msg[160];
+        std::snprintf(msg, sizeof msg, "cuTensorMapEncodeTiled (3-D B chunks) failed (%d)", static_cast<int>(r));
+        return fail(h, GEMM_ERR_CUDA, msg);
+    }
+    return GEMM_OK;
+}
+
 class DeviceGuard {
   public:
     explicit DeviceGuard(int dev)
@@ -301,14 +326,17 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
         const int bk = dg::tc_bk(es);
         rc = encode_2d(h, &tmA, es, A, K, M, lda, bk, dg::kTcBM);
         if (rc) return rc;
-        if (layout_b == GEMM_B_ROW_MAJOR)
-            // MN-major B; 32-bit elements need 32-byte swizzle atoms there.
-            rc = encode_2d(h, &tmB, es, B, N, K, ldb, 128 / es, bk,
-                           es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B);
+        const int cluster = h->tc_cluster >= 2 && M > dg::kTcBM ? h->tc_cluster : 1;
+        // MN-major B; 32-bit elements need 32-byte swizzle atoms there.
+        const CUtensorMapSwizzle b_swz = es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B;
+        const bool b_chunks = layout_b == GEMM_B_ROW_MAJOR && cluster == 3 && N % (128 / es) == 0;
+        if (b_chunks)
+            rc = encode_b_chunks(h, &tmB, es, B, N, K, ldb, bk, (dg::kTcBN / 2) / (128 / es), b_swz);
+        else if (layout_b == GEMM_B_ROW_MAJOR)
+            rc = encode_2d(h, &tmB, es, B, N, K, ldb, 128 / es, bk, b_swz);
         else
             rc = encode_2d(h, &tmB, es, B, K, N, ldb, bk, dg::kTcBoxBCol);
         if (rc) return rc;
-        const int cluster = h->tc_cluster >= 2 && M > dg::kTcBM ? h->tc_cluster : 1;
         int grid = dg::tc_grid(M, N, h->max_ctas > 0 ? h->max_ctas : h->sm_count, cluster);
         lc.grid = grid;
         lc.group_m = h->tc_group_m;
@@ -319,10 +347,12 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
             if (rc) return rc;
         }
         cudaError_t e = dg::launch_tc(dtype, layout_b, tmA, tmB, c_tma ? &tmC : nullptr, static_cast<int>(M),
-                                      static_cast<int>(N), static_cast<int>(K), C, ldc, c_vec4, lc, cluster);
+                                      static_cast<int>(N), static_cast<int>(K), C, ldc, c_vec4, lc, cluster,
+                                      b_chunks);
         if (e != cudaSuccess) return cuda_fail(h, e, "tensor-core kernel launch");
         path = std::string(dtype == GEMM_BF16 ? "tc_bf16" : "tc_tf32") +
-               (cluster == 3 ? "_pair256x256_" : "_128x256_") + lay + (cluster == 2 ? "_cluster2" : "") + path;
+               (cluster == 3 ? "_pair256x256_" : "_128x256_") + lay + (cluster == 2 ? "_cluster2" : "") +
+               (b_chunks ? "+b3d" : "") + path;
     }
     ++h->launches;
     h->last_path = path;

@@ -65,6 +65,7 @@ struct TcParams {
     unsigned long long timeout_ns;
     int c_vec4;
     int c_tma;       // 1: C is written by TMA stores through tmC
+    int b_chunks;    // 1 (pair kernel, row-major B): tmB is the 3-D chunk view, one box per stage
     int debug_drop;  // test hook: CTA 0 never loads its first stage
 };
 
@@ -482,9 +483,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tma_load_2d_pair(a_st, &tmA, fb, kt * BK, mb * BM);
                     const int n_half = nb * BN + static_cast<int>(rank) * (BN / 2);
                     if (LAYOUT_B == 0) {
+                        if (p.b_chunks) {
+                            // {column in chunk, k, chunk}: the B_HALF_BOXES chunks of
+                            // this CTA's half land one after another, as the 2-D
+                            // boxes would (the swizzle follows the address)
+                            tma_load_3d_pair(b_st, &tmB, fb, 0, kt * BK, n_half / BOX_N);
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < B_HALF_BOXES; ++j)
-                            tma_load_2d_pair(b_st + j * BOX_BYTES, &tmB, fb, n_half + j * BOX_N, kt * BK);
+                            for (int j = 0; j < B_HALF_BOXES; ++j)
+                                tma_load_2d_pair(b_st + j * BOX_BYTES, &tmB, fb, n_half + j * BOX_N, kt * BK);
+                        }
                     } else {
                         tma_load_2d_pair(b_st, &tmB, fb, kt * BK, n_half);
                     }
@@ -723,7 +731,7 @@ int tc_grid(int64_t M, int64_t N, int sm_count, int cluster)
 
 cudaError_t launch_tc(int dtype, int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB,
                       const CUtensorMap *tmC, int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
-                      const LaunchCommon &lc, int cluster)
+                      const LaunchCommon &lc, int cluster, bool b_chunks)
 {
     TcParams p;
     p.M = M;
@@ -740,6 +748,7 @@ cudaError_t launch_tc(int dtype, int layout_b, const CUtensorMap &tmA, const CUt
     p.timeout_ns = lc.timeout_ns;
     p.c_vec4 = c_vec4 ? 1 : 0;
     p.c_tma = tmC != nullptr ? 1 : 0;
+    p.b_chunks = b_chunks && cluster == 3 && layout_b == 0 ? 1 : 0;
     p.debug_drop = lc.debug_drop;
     const CUtensorMap &tc = tmC != nullptr ? *tmC : tmA;  // unused when c_tma == 0
     const bool bf16 = dtype == GEMM_BF16;

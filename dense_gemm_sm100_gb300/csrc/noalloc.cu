@@ -178,7 +178,7 @@ extern "C" int gemm_run_noalloc(int layout_b, int64_t M, int64_t N, int64_t K, c
         if (!ok) return GEMM_ERR_CUDA;
         lc.grid = dg::tc_grid(M, N, s->sm_count, 1);
         e = dg::launch_tc(dtype, layout_b, tmA, tmB, nullptr, static_cast<int>(M), static_cast<int>(N),
-                          static_cast<int>(K), C, ldc, c_vec4, lc, 1);
+                          static_cast<int>(K), C, ldc, c_vec4, lc, 1, false);
     }
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

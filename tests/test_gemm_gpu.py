@@ -350,7 +350,8 @@ def test_launch_count_increments(g):
 # ------------------------------------------------------- clustered tensor-core kernel
 
 CLUSTER_SHAPES = [(129, 257, 33), (257, 600, 64), (300, 520, 260), (385, 300, 100),
-                  (1000, 40, 300), (640, 1024, 512)]
+                  (1000, 40, 300), (640, 1024, 512),
+                  (300, 448, 96)]  # whole 128-byte chunks of B, the last box half past N
 
 
 @pytest.mark.parametrize("cluster_mode", [2, 3])
@@ -372,6 +373,10 @@ def test_cluster_pairs_match_oracle_and_single_cta(g, oracle_mod, cluster_mode, 
     try:
         C2 = run_gpu(g, A, B, layout, mode).cpu()
         assert ("cluster2" if cluster_mode == 2 else "pair256x256") in g.last_path
+        # pair MMA with row-major B: one 3-D TMA box per stage when N is whole chunks
+        chunk = 64 if mode == "bf16" else 32
+        b3d = cluster_mode == 3 and layout == ROW and M > 128 and N % chunk == 0
+        assert ("+b3d" in g.last_path) == b3d, g.last_path
     finally:
         g.set_option(gemm.GEMM_OPT_TC_CLUSTER, 3)
     Cr, S = oracle_of(oracle_mod, A, B, layout)
