@@ -46,9 +46,9 @@ NOMINAL_PF = {"bf16": 2.25, "tf32": 1.1}
 # ncu capture of the kernel as it is now; None until captured for this version.
 # Key: workload name -> (bytes per launch, summary file under profiles/).
 NCU_TRAFFIC: dict[str, tuple[float, str]] = {
-    "fp32_8192_row": (2715.4e6 + 260.6e6, "profiles/dram_traffic_full_size.md"),
-    "ffn_bf16_8192x14336x4096": (594.6e6 + 433.4e6, "profiles/dram_traffic_full_size.md"),
-    "ffn_tf32_8192x14336x4096": (1824.8e6 + 449.5e6, "profiles/dram_traffic_full_size.md"),
+    "fp32_8192_row": (2715.3e6 + 260.5e6, "profiles/dram_traffic_full_size.md"),
+    "ffn_bf16_8192x14336x4096": (592.1e6 + 432.5e6, "profiles/dram_traffic_full_size.md"),
+    "ffn_tf32_8192x14336x4096": (1836.4e6 + 445.5e6, "profiles/dram_traffic_full_size.md"),
 }
 
 DESCRIPTIONS = {
