@@ -125,18 +125,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// Same, with an L2 cache-eviction policy (from createpolicy).
-__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map,
-                                                 uint32_t bar, int32_t x, int32_t y,
-                                                 uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
-        : "memory");
-}
-
 // Same box, written to the same shared-memory offset in every CTA of the
 // cluster named in cta_mask; each destination's mbarrier (same offset) gets
 // the transaction bytes.
@@ -239,13 +227,6 @@ __device__ __forceinline__ void cluster_sync()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_last()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
 }
 
 // ---------------------------------------------------------------- tcgen05
