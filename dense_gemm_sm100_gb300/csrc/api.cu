@@ -329,9 +329,10 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
         const int cluster = h->tc_cluster >= 2 && M > dg::kTcBM ? h->tc_cluster : 1;
         // MN-major B; 32-bit elements need 32-byte swizzle atoms there.
         const CUtensorMapSwizzle b_swz = es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B;
-        const bool b_chunks = layout_b == GEMM_B_ROW_MAJOR && cluster == 3 && N % (128 / es) == 0;
+        const bool b_chunks = layout_b == GEMM_B_ROW_MAJOR && cluster != 2 && N % (128 / es) == 0;
         if (b_chunks)
-            rc = encode_b_chunks(h, &tmB, es, B, N, K, ldb, bk, (dg::kTcBN / 2) / (128 / es), b_swz);
+            rc = encode_b_chunks(h, &tmB, es, B, N, K, ldb, bk, (cluster == 3 ? dg::kTcBN / 2 : dg::kTcBN) / (128 / es),
+                                 b_swz);
         else if (layout_b == GEMM_B_ROW_MAJOR)
             rc = encode_2d(h, &tmB, es, B, N, K, ldb, 128 / es, bk, b_swz);
         else

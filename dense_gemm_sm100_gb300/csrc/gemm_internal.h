@@ -86,9 +86,10 @@ cudaError_t launch_simt_tail_reduce(int config, int layout_b, int M, int N, int 
 // pairs that share (multicast) the B tile; cluster = 3 runs the pair MMA
 // (cta_group::2, 256x256 per pair); lc.grid must then be even.
 constexpr int kTcBoxC = 32;
-// b_chunks (pair MMA, row-major B only): tmB is the 3-D view {128-byte
-// column chunk, K, chunk index} with a box of kTcBN/2 columns, fetched by one
-// TMA instruction per stage instead of one per chunk.
+// b_chunks (row-major B; one-CTA or pair MMA mode): tmB is the 3-D view
+// {128-byte column chunk, K, chunk index} with a box of the columns one CTA
+// stages (kTcBN, or kTcBN/2 in a pair), fetched by one TMA instruction per
+// stage instead of one per chunk.
 cudaError_t launch_tc(int dtype, int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB,
                       const CUtensorMap *tmC, int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
                       const LaunchCommon &lc, int cluster, bool b_chunks);

@@ -65,7 +65,7 @@ struct TcParams {
     unsigned long long timeout_ns;
     int c_vec4;
     int c_tma;       // 1: C is written by TMA stores through tmC
-    int b_chunks;    // 1 (pair kernel, row-major B): tmB is the 3-D chunk view, one box per stage
+    int b_chunks;    // 1 (row-major B, one-CTA or pair kernel): tmB is the 3-D chunk view, one box per stage
     int debug_drop;  // test hook: CTA 0 never loads its first stage
 };
 
@@ -194,7 +194,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (p.debug_drop && blockIdx.x == 0 && it == 0) continue;  // bytes that never come
                     tma_load_2d(a_st, &tmA, fb, kt * BK, mb * BM);
                     if (LAYOUT_B == 0) {
-                        if (CL == 1) {
+                        if (CL == 1 && p.b_chunks) {
+                            tma_load_3d(b_st, &tmB, fb, 0, kt * BK, nb * BN / BOX_N);  // all B_BOXES chunks
+                        } else if (CL == 1) {
 #pragma unroll
                             for (int j = 0; j < B_BOXES; ++j)
                                 tma_load_2d(b_st + j * BOX_BYTES, &tmB, fb, nb * BN + j * BOX_N, kt * BK);
@@ -748,7 +750,7 @@ cudaError_t launch_tc(int dtype, int layout_b, const CUtensorMap &tmA, const CUt
     p.timeout_ns = lc.timeout_ns;
     p.c_vec4 = c_vec4 ? 1 : 0;
     p.c_tma = tmC != nullptr ? 1 : 0;
-    p.b_chunks = b_chunks && cluster == 3 && layout_b == 0 ? 1 : 0;
+    p.b_chunks = b_chunks && (cluster == 3 || cluster == 1) && layout_b == 0 ? 1 : 0;
     p.debug_drop = lc.debug_drop;
     const CUtensorMap &tc = tmC != nullptr ? *tmC : tmA;  // unused when c_tma == 0
     const bool bf16 = dtype == GEMM_BF16;

@@ -377,6 +377,10 @@ def test_cluster_pairs_match_oracle_and_single_cta(g, oracle_mod, cluster_mode, 
         chunk = 64 if mode == "bf16" else 32
         b3d = cluster_mode == 3 and layout == ROW and M > 128 and N % chunk == 0
         assert ("+b3d" in g.last_path) == b3d, g.last_path
+        # the one-CTA run above used the 3-D box under the same condition
+        g.set_option(gemm.GEMM_OPT_TC_CLUSTER, 1)
+        run_gpu(g, A, B, layout, mode)
+        assert ("+b3d" in g.last_path) == (layout == ROW and N % chunk == 0), g.last_path
     finally:
         g.set_option(gemm.GEMM_OPT_TC_CLUSTER, 3)
     Cr, S = oracle_of(oracle_mod, A, B, layout)
