@@ -119,9 +119,14 @@ struct PackPlan {
     size_t a_bytes = 0, b_bytes = 0;
     int simt_config = 0;
     dg::SplitK split;     // partials pointer is filled in by run_device
-    size_t split_bytes = 0;
+    dg::TcSplit tc_split; // tensor-core K split (partials filled in by run_device)
+    size_t split_bytes = 0;  // partial tiles of either split
     size_t total() const { return a_bytes + b_bytes + split_bytes; }
 };
+
+// Tensor-core mode for an M-row problem: the configured CTA-pair mode needs
+// more than one 128-row tile row.
+int tc_cluster_for(const gemm_ctx *h, int64_t M) { return h->tc_cluster >= 2 && M > dg::kTcBM ? h->tc_cluster : 1; }
 
 PackPlan plan_pack(const gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K,
                    const void *A, int64_t lda, const void *B, int64_t ldb, int dtype)
@@ -154,6 +159,15 @@ PackPlan plan_pack(const gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_
         }
         pp.split_bytes = static_cast<size_t>(
             round_up(static_cast<int64_t>(dg::simt_partial_bytes(pp.simt_config, layout_b, pp.split)), 256));
+    } else {
+        const int cluster = tc_cluster_for(h, M);
+        if (cluster != 2) {
+            const int64_t ctas = h->max_ctas > 0 ? h->max_ctas : h->sm_count;
+            const int64_t slots = cluster == 3 ? ctas / 2 : ctas;
+            pp.tc_split = dg::tc_pick_splits(dg::tc_units(M, N, cluster), slots, K, es, h->split_k);
+            pp.split_bytes = static_cast<size_t>(
+                round_up(static_cast<int64_t>(dg::tc_partial_bytes(M, N, pp.tc_split)), 256));
+        }
     }
     return pp;
 }
@@ -326,7 +340,7 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
         const int bk = dg::tc_bk(es);
         rc = encode_2d(h, &tmA, es, A, K, M, lda, bk, dg::kTcBM);
         if (rc) return rc;
-        const int cluster = h->tc_cluster >= 2 && M > dg::kTcBM ? h->tc_cluster : 1;
+        const int cluster = tc_cluster_for(h, M);
         // MN-major B; 32-bit elements need 32-byte swizzle atoms there.
         const CUtensorMapSwizzle b_swz = es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B;
         const bool b_chunks = layout_b == GEMM_B_ROW_MAJOR && cluster != 2 && N % (128 / es) == 0;
@@ -338,22 +352,32 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
         else
             rc = encode_2d(h, &tmB, es, B, K, N, ldb, bk, dg::kTcBoxBCol);
         if (rc) return rc;
-        int grid = dg::tc_grid(M, N, h->max_ctas > 0 ? h->max_ctas : h->sm_count, cluster);
+        dg::TcSplit sp = pp.tc_split;
+        if (sp.splits > 1) sp.partials = reinterpret_cast<float *>(ws + pp.a_bytes + pp.b_bytes);
+        int grid = dg::tc_grid(M, N, h->max_ctas > 0 ? h->max_ctas : h->sm_count, cluster, sp.splits);
         lc.grid = grid;
         lc.group_m = h->tc_group_m;
         alignas(64) CUtensorMap tmC;
-        const bool c_tma = c_vec4 && h->tc_tma_store;
+        const bool c_tma = c_vec4 && h->tc_tma_store && sp.splits == 1;
         if (c_tma) {
             rc = encode_2d(h, &tmC, 4, C, N, M, ldc, dg::kTcBoxC, dg::kTcBoxC);
             if (rc) return rc;
         }
         cudaError_t e = dg::launch_tc(dtype, layout_b, tmA, tmB, c_tma ? &tmC : nullptr, static_cast<int>(M),
                                       static_cast<int>(N), static_cast<int>(K), C, ldc, c_vec4, lc, cluster,
-                                      b_chunks);
+                                      b_chunks, sp);
         if (e != cudaSuccess) return cuda_fail(h, e, "tensor-core kernel launch");
         path = std::string(dtype == GEMM_BF16 ? "tc_bf16" : "tc_tf32") +
                (cluster == 3 ? "_pair256x256_" : "_128x256_") + lay + (cluster == 2 ? "_cluster2" : "") +
                (b_chunks ? "+b3d" : "") + path;
+        if (sp.splits > 1) {
+            ++h->launches;
+            e = dg::launch_tile_split_reduce(sp.partials, sp.splits, (M + dg::kTcBM - 1) / dg::kTcBM,
+                                             (N + dg::kTcBN - 1) / dg::kTcBN, dg::kTcBM, dg::kTcBN, C, ldc, M, N,
+                                             c_vec4, h->sm_count, stream);
+            if (e != cudaSuccess) return cuda_fail(h, e, "split-K reduction launch");
+            path += "+splitk" + std::to_string(sp.splits);
+        }
     }
     ++h->launches;
     h->last_path = path;

@@ -6,6 +6,9 @@
 //    16-byte aligned rows).  One CTA walks whole rows: reads and writes are
 //    both row-contiguous, so every warp access is coalesced ("PMPP Chapter 06:
 //    Performance considerations", section 1, coalescing).
+//  * tile split reduction: C = the K-slice partial tiles of the tensor-core
+//    kernels added in slice order ("GEMM 性能优化", 台阶 1: partial sums over K
+//    slices add up to the product).
 //  * zero fill: C = 0 for K = 0 (the empty sum).
 #include <cstdint>
 
@@ -35,6 +38,44 @@ __global__ void __launch_bounds__(256) zero_fill_kernel(float *__restrict__ C, l
     }
 }
 
+// One thread per 4 consecutive columns of a tile row; slices added in order.
+__global__ void __launch_bounds__(256) tile_split_reduce_kernel(const float *__restrict__ P, int splits,
+                                                                long long tiles_m, long long tiles_n, int bm,
+                                                                int bn, float *__restrict__ C, long long ldc,
+                                                                long long M, long long N, int c_vec4)
+{
+    const long long tile = (long long)bm * bn;
+    const long long quads = tiles_m * tiles_n * (tile / 4);
+    const long long slice = tiles_m * tiles_n * tile;
+    for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < quads;
+         q += (long long)gridDim.x * blockDim.x) {
+        const long long t = q / (tile / 4);
+        const long long e = (q - t * (tile / 4)) * 4;
+        const long long mb = t / tiles_n, nb = t - (t / tiles_n) * tiles_n;
+        const long long m = mb * bm + e / bn;
+        const long long n = nb * bn + e % bn;
+        if (m >= M || n >= N) continue;
+        const float *src = P + t * tile + e;
+        float4 acc = *reinterpret_cast<const float4 *>(src);
+        for (int s = 1; s < splits; ++s) {
+            const float4 v = *reinterpret_cast<const float4 *>(src + s * slice);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        float *c = C + m * ldc + n;
+        if (c_vec4 && n + 3 < N) {
+            *reinterpret_cast<float4 *>(c) = acc;
+        } else {
+            c[0] = acc.x;
+            if (n + 1 < N) c[1] = acc.y;
+            if (n + 2 < N) c[2] = acc.z;
+            if (n + 3 < N) c[3] = acc.w;
+        }
+    }
+}
+
 int rows_grid(long long rows, int sm_count)
 {
     const long long cap = static_cast<long long>(sm_count > 0 ? sm_count : 1) * 8;
@@ -54,6 +95,20 @@ cudaError_t launch_repack(const void *src, int64_t lds, void *dst, int64_t ldd, 
     else
         repack_rows_kernel<uint16_t><<<grid, 256, 0, stream>>>(
             static_cast<const uint16_t *>(src), lds, static_cast<uint16_t *>(dst), ldd, rows, cols);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tile_split_reduce(const float *partials, int splits, int64_t tiles_m, int64_t tiles_n, int bm,
+                                     int bn, float *C, int64_t ldc, int64_t M, int64_t N, bool c_vec4, int sm_count,
+                                     cudaStream_t stream)
+{
+    if (M <= 0 || N <= 0 || splits < 1) return cudaSuccess;
+    const long long quads = tiles_m * tiles_n * ((long long)bm * bn / 4);
+    long long blocks = (quads + 255) / 256;
+    const long long cap = 8LL * (sm_count > 0 ? sm_count : 1);
+    if (blocks > cap) blocks = cap;
+    tile_split_reduce_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(partials, splits, tiles_m, tiles_n, bm, bn,
+                                                                            C, ldc, M, N, c_vec4 ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -86,16 +86,39 @@ cudaError_t launch_simt_tail_reduce(int config, int layout_b, int M, int N, int 
 // pairs that share (multicast) the B tile; cluster = 3 runs the pair MMA
 // (cta_group::2, 256x256 per pair); lc.grid must then be even.
 constexpr int kTcBoxC = 32;
+// K split of the tensor-core kernels (modes 1 and 3): every tile unit is cut
+// into `splits` slices of kt_per_split stages; slice s of tile (mb, nb) goes
+// to partials + ((s*tiles_m + mb)*tiles_n + nb)*kTcBM*kTcBN (row-major
+// 128 x 256 floats) and launch_tile_split_reduce adds the slices into C.
+struct TcSplit {
+    int splits = 1;
+    int kt_per_split = 0;
+    float *partials = nullptr;
+};
+// Slices for a launch of `units` tile units on `slots` unit slots (CTAs, or
+// CTA pairs in mode 3) when they fill at most a third of a wave: 3 to 16
+// slices of at least four stages each (want > 1 forces that many).
+TcSplit tc_pick_splits(int64_t units, int64_t slots, int64_t K, int elem_bytes, int want);
+size_t tc_partial_bytes(int64_t M, int64_t N, const TcSplit &sp);
+
 // b_chunks (row-major B; one-CTA or pair MMA mode): tmB is the 3-D view
 // {128-byte column chunk, K, chunk index} with a box of the columns one CTA
 // stages (kTcBN, or kTcBN/2 in a pair), fetched by one TMA instruction per
 // stage instead of one per chunk.
 cudaError_t launch_tc(int dtype, int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB,
                       const CUtensorMap *tmC, int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
-                      const LaunchCommon &lc, int cluster, bool b_chunks);
+                      const LaunchCommon &lc, int cluster, bool b_chunks, const TcSplit &sp = TcSplit());
 
 // Persistent grid of the tensor-core kernel: one CTA per SM, whole clusters.
-int tc_grid(int64_t M, int64_t N, int sm_count, int cluster);
+int tc_grid(int64_t M, int64_t N, int sm_count, int cluster, int splits = 1);
+// Tile units of a tensor-core launch (tiles, or tile pairs in mode 3).
+int64_t tc_units(int64_t M, int64_t N, int cluster);
+
+// C[m][n] = sum over s of partials[s][mb][nb][m % bm][n % bn], slices added in
+// order s = 0, 1, ... (deterministic), for m < M, n < N.
+cudaError_t launch_tile_split_reduce(const float *partials, int splits, int64_t tiles_m, int64_t tiles_n, int bm,
+                                     int bn, float *C, int64_t ldc, int64_t M, int64_t N, bool c_vec4, int sm_count,
+                                     cudaStream_t stream);
 
 // dst[r*ldd + c] = src[r*lds + c] for r < rows, c < cols (elem_bytes 2 or 4).
 cudaError_t launch_repack(const void *src, int64_t lds, void *dst, int64_t ldd, int64_t rows,

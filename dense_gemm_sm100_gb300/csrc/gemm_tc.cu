@@ -67,7 +67,27 @@ struct TcParams {
     int c_tma;       // 1: C is written by TMA stores through tmC
     int b_chunks;    // 1 (row-major B, one-CTA or pair kernel): tmB is the 3-D chunk view, one box per stage
     int debug_drop;  // test hook: CTA 0 never loads its first stage
+    // K split: units are (tile unit, slice) slice-major; slice s covers
+    // stages [s*kt_per_split, min(k_tiles, (s+1)*kt_per_split)) and its
+    // accumulator goes to partials[s][tile row][tile column] (BM x BN floats)
+    int splits, kt_per_split;
+    float *partials;
 };
+
+// K range of work unit u; `base` = tile units per slice.
+struct KRange {
+    int ub, kt0, kt1, slice;
+};
+
+__device__ __forceinline__ KRange unit_krange(int u, const TcParams &p, int base, int k_tiles)
+{
+    KRange r;
+    r.slice = u / base;
+    r.ub = u - r.slice * base;
+    r.kt0 = r.slice * p.kt_per_split;
+    r.kt1 = min(k_tiles, r.kt0 + p.kt_per_split);
+    return r;
+}
 
 // Unit u of the grouped order over (tile-row groups of CL tiles) x tiles_n:
 // groups of `group_m` units along M, column-major inside a group, so CTAs
@@ -139,7 +159,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
     const int cluster = blockIdx.x / CL;
     const int clusters = gridDim.x / CL;
-    const int num_units = ((p.tiles_m + CL - 1) / CL) * p.tiles_n;
+    const int base_units = ((p.tiles_m + CL - 1) / CL) * p.tiles_n;
+    const int num_units = base_units * p.splits;
     const int k_tiles = (p.K + BK - 1) / BK;
 
     if (threadIdx.x == 0) {
@@ -175,9 +196,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int u = cluster; ok && u < num_units; u += clusters) {
+                const KRange kr = unit_krange(u, p, base_units, k_tiles);
                 int mb, nb;
-                unit_coords<CL>(u, p, rank, mb, nb);
-                for (int kt = 0; kt < k_tiles; ++kt, ++it) {
+                unit_coords<CL>(kr.ub, p, rank, mb, nb);
+                for (int kt = kr.kt0; kt < kr.kt1; ++kt, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
                     if (!mbar_wait(empty_bar + 8 * s, ph ^ 1u, abort_flag, p.status,
@@ -251,7 +273,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + abuf * BN;
-                for (int kt = 0; kt < k_tiles; ++kt, ++it) {
+                const KRange kr = unit_krange(u, p, base_units, k_tiles);
+                for (int kt = kr.kt0; kt < kr.kt1; ++kt, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
                     if (!mbar_wait(full_bar + 8 * s, ph, abort_flag, p.status, kWaitMmaFull,
@@ -269,7 +292,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             LAYOUT_B == 0
                                 ? smem_desc(b_st + kk * UMMA_K * 128, BOX_BYTES, B_MN_SBO, B_MN_LAYOUT)
                                 : smem_desc(b_st + kk * 32, 16, 1024, kLayoutSw128);
-                        const uint32_t accumulate = (kt > 0 || kk > 0) ? 1u : 0u;
+                        const uint32_t accumulate = (kt > kr.kt0 || kk > 0) ? 1u : 0u;
                         if (DT == 0)
                             tc_mma_f16(d_tmem, adesc, bdesc, IDESC, accumulate);
                         else
@@ -299,8 +322,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (p.c_tma && lane == 0) tma_prefetch_desc(&tmC);
         uint32_t acc_it = 0;
         for (int u = cluster; u < num_units; u += clusters, ++acc_it) {
+            const KRange kr = unit_krange(u, p, base_units, k_tiles);
             int mb, nb;
-            unit_coords<CL>(u, p, rank, mb, nb);
+            unit_coords<CL>(kr.ub, p, rank, mb, nb);
             const uint32_t abuf = acc_it & 1u;
             const uint32_t aph = (acc_it >> 1) & 1u;
             bool ok = true;
@@ -325,7 +349,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (lane == 0) mbar_arrive(tempty_bar + 8 * abuf);
                 }
                 const int n0 = nb * BN + c * 32;
-                if (p.c_tma) {
+                if (p.splits > 1) {
+                    // a K slice: the whole partial tile (rows and columns past
+                    // M and N hold zeros), added into C by the reduction kernel
+                    if (mb < p.tiles_m) {
+                        float *prow = p.partials +
+                                      (((long long)kr.slice * p.tiles_m + mb) * p.tiles_n + nb) * (BM * BN) +
+                                      row * BN + c * 32;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            *reinterpret_cast<float4 *>(prow + 4 * j) =
+                                make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                            __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                    }
+                } else if (p.c_tma) {
                     // Row `lane` of a 32x32 chunk, 128-byte swizzled (chunk j
                     // of row r at 16*(j ^ (r & 7))), then one TMA store of the
                     // chunk; TMA drops the rows and columns outside C.
@@ -433,7 +470,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const bool leader = rank == 0;
     const int cluster = blockIdx.x / 2;
     const int clusters = gridDim.x / 2;
-    const int num_units = ((p.tiles_m + 1) / 2) * p.tiles_n;
+    const int base_units = ((p.tiles_m + 1) / 2) * p.tiles_n;
+    const int num_units = base_units * p.splits;
     const int k_tiles = (p.K + BK - 1) / BK;
 
     if (threadIdx.x == 0) {
@@ -466,9 +504,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int u = cluster; ok && u < num_units; u += clusters) {
+                const KRange kr = unit_krange(u, p, base_units, k_tiles);
                 int mb, nb;
-                unit_coords<2>(u, p, rank, mb, nb);
-                for (int kt = 0; kt < k_tiles; ++kt, ++it) {
+                unit_coords<2>(kr.ub, p, rank, mb, nb);
+                for (int kt = kr.kt0; kt < kr.kt1; ++kt, ++it) {
                     const uint32_t s = it % P_STAGES;
                     const uint32_t ph = (it / P_STAGES) & 1u;
                     if (!mbar_wait(empty_bar + 8 * s, ph ^ 1u, abort_flag, p.status,
@@ -533,7 +572,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + abuf * BN;
-                for (int kt = 0; kt < k_tiles; ++kt, ++it) {
+                const KRange kr = unit_krange(u, p, base_units, k_tiles);
+                for (int kt = kr.kt0; kt < kr.kt1; ++kt, ++it) {
                     const uint32_t s = it % P_STAGES;
                     const uint32_t ph = (it / P_STAGES) & 1u;
                     if (!mbar_wait(full_bar + 8 * s, ph, abort_flag, p.status, kWaitMmaFull,
@@ -551,7 +591,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             LAYOUT_B == 0
                                 ? smem_desc(b_st + kk * UMMA_K * 128, BOX_BYTES, B_MN_SBO, B_MN_LAYOUT)
                                 : smem_desc(b_st + kk * 32, 16, 1024, kLayoutSw128);
-                        const uint32_t accumulate = (kt > 0 || kk > 0) ? 1u : 0u;
+                        const uint32_t accumulate = (kt > kr.kt0 || kk > 0) ? 1u : 0u;
                         if (DT == 0)
                             tc_mma_f16_pair(d_tmem, adesc, bdesc, IDESC, accumulate);
                         else
@@ -577,8 +617,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (p.c_tma && lane == 0) tma_prefetch_desc(&tmC);
         uint32_t acc_it = 0;
         for (int u = cluster; u < num_units; u += clusters, ++acc_it) {
+            const KRange kr = unit_krange(u, p, base_units, k_tiles);
             int mb, nb;
-            unit_coords<2>(u, p, rank, mb, nb);
+            unit_coords<2>(kr.ub, p, rank, mb, nb);
             const uint32_t abuf = acc_it & 1u;
             const uint32_t aph = (acc_it >> 1) & 1u;
             bool ok = true;
@@ -607,7 +648,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
                 const int n0 = nb * BN + c * 32;
-                if (p.c_tma) {
+                if (p.splits > 1) {
+                    // a K slice: this CTA's 128 rows of the partial tile (the
+                    // odd CTA of a last pair past M writes nothing)
+                    if (mb < p.tiles_m) {
+                        float *prow = p.partials +
+                                      (((long long)kr.slice * p.tiles_m + mb) * p.tiles_n + nb) * (BM * BN) +
+                                      row * BN + c * 32;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            *reinterpret_cast<float4 *>(prow + 4 * j) =
+                                make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                            __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                    }
+                } else if (p.c_tma) {
                     const uint32_t buf = stage_buf + static_cast<uint32_t>(c & 1) * EPI_CHUNK_BYTES;
                     if (lane == 0) bulk_wait_group_read<1>();
                     __syncwarp();
@@ -722,18 +776,57 @@ cudaError_t prepare_tc()
     return e;
 }
 
-int tc_grid(int64_t M, int64_t N, int sm_count, int cluster)
+int64_t tc_units(int64_t M, int64_t N, int cluster)
 {
     const int64_t tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
     const int cl = cluster >= 2 ? 2 : 1;
-    const int64_t units = ((tiles_m + cl - 1) / cl) * tiles_n;
+    return ((tiles_m + cl - 1) / cl) * tiles_n;
+}
+
+int tc_grid(int64_t M, int64_t N, int sm_count, int cluster, int splits)
+{
+    const int cl = cluster >= 2 ? 2 : 1;
+    const int64_t units = tc_units(M, N, cluster) * (splits > 1 ? splits : 1);
     const int64_t clusters = sm_count >= cl ? sm_count / cl : 1;
     return static_cast<int>(cl * (units < clusters ? units : clusters));
 }
 
+TcSplit tc_pick_splits(int64_t units, int64_t slots, int64_t K, int elem_bytes, int want)
+{
+    // Wave model ("GEMM 性能优化", Wave 模型): tile units that fill less than
+    // one wave are cut along K so that units x slices fills it.
+    TcSplit sp;
+    const int64_t k_tiles = (K + (128 / elem_bytes) - 1) / (128 / elem_bytes);
+    int64_t s;
+    if (want > 1) {
+        s = want < k_tiles ? want : k_tiles;
+    } else {
+        if (want == 1 || units <= 0 || units >= slots) return sp;
+        s = slots / units;
+        s = s < k_tiles / 4 ? s : k_tiles / 4;
+        s = s < 16 ? s : 16;
+        // Two slices do not pay for the second launch and the partial tiles
+        // (BF16 128 x 14336 x 4096: 35.0 us whole, 38.9 us in two slices).
+        if (s < 3) return sp;
+    }
+    if (s <= 1) return sp;
+    const int64_t kt_per = (k_tiles + s - 1) / s;
+    sp.splits = static_cast<int>((k_tiles + kt_per - 1) / kt_per);  // no empty slice
+    sp.kt_per_split = static_cast<int>(kt_per);
+    if (sp.splits <= 1) return TcSplit();
+    return sp;
+}
+
+size_t tc_partial_bytes(int64_t M, int64_t N, const TcSplit &sp)
+{
+    if (sp.splits <= 1) return 0;
+    const int64_t tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
+    return static_cast<size_t>(sp.splits) * tiles_m * tiles_n * BM * BN * sizeof(float);
+}
+
 cudaError_t launch_tc(int dtype, int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB,
                       const CUtensorMap *tmC, int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
-                      const LaunchCommon &lc, int cluster, bool b_chunks)
+                      const LaunchCommon &lc, int cluster, bool b_chunks, const TcSplit &sp)
 {
     TcParams p;
     p.M = M;
@@ -752,6 +845,11 @@ cudaError_t launch_tc(int dtype, int layout_b, const CUtensorMap &tmA, const CUt
     p.c_tma = tmC != nullptr ? 1 : 0;
     p.b_chunks = b_chunks && (cluster == 3 || cluster == 1) && layout_b == 0 ? 1 : 0;
     p.debug_drop = lc.debug_drop;
+    const bool split = sp.splits > 1 && cluster != 2;
+    p.splits = split ? sp.splits : 1;
+    p.kt_per_split = split ? sp.kt_per_split : (K + (128 / (dtype == GEMM_BF16 ? 2 : 4)) - 1) / (128 / (dtype == GEMM_BF16 ? 2 : 4));
+    if (p.kt_per_split < 1) p.kt_per_split = 1;
+    p.partials = split ? sp.partials : nullptr;
     const CUtensorMap &tc = tmC != nullptr ? *tmC : tmA;  // unused when c_tma == 0
     const bool bf16 = dtype == GEMM_BF16;
     if (cl == 3) {

@@ -87,10 +87,11 @@ extern "C" {
  * with 16 consumer warps, 256x128 with 16 consumer warps.  A configuration
  * the device cannot run is refused with GEMM_ERR_INVALID. */
 #define GEMM_OPT_SIMT_CONFIG 6
-/* FP32 K slices.  0 = chosen per shape: the tiles of a partial last wave
- * (all tiles when they fill less than one wave) are cut into K slices that
- * a second kernel adds in slice order.  1 = never.  2..64 = every tile cut
- * into that many slices (fewer if K is short). */
+/* K slices.  0 = chosen per shape.  FP32: the tiles of a partial last wave
+ * (all tiles when they fill less than one wave) are cut into K slices;
+ * tensor cores (one-CTA and pair modes): all tiles when they fill less than
+ * one wave.  A second kernel adds the slices in slice order.  1 = never.
+ * 2..64 = every tile cut into that many slices (fewer if K is short). */
 #define GEMM_OPT_SPLIT_K 7
 #define GEMM_OPT_TC_CLUSTER 8     /* tensor-core mode: 1 one CTA per tile, 2 CTA pairs sharing B by multicast, 3 pair MMA (cta_group::2, default) */
 #define GEMM_OPT_TC_TMA_STORE 9   /* 1 (default): tensor-core epilogue stores C by TMA when aligned */

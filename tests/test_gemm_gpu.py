@@ -188,12 +188,14 @@ def test_tma_store_epilogue_matches_thread_stores(g, mode, shape):
     dev = torch.device("cuda", 0)
     big = torch.full((M, N + 12), float("nan"), device=dev)  # ldc = N + 12 keeps 16-byte rows
     C_tma = big[:, :N]
-    run_gpu(g, A, B, ROW, mode, C=C_tma)
-    g.set_option(gemm.GEMM_OPT_TC_TMA_STORE, 0)
+    g.set_option(gemm.GEMM_OPT_SPLIT_K, 1)  # a K split would write C from its reduction kernel
     try:
+        run_gpu(g, A, B, ROW, mode, C=C_tma)
+        g.set_option(gemm.GEMM_OPT_TC_TMA_STORE, 0)
         C_thr = run_gpu(g, A, B, ROW, mode).cpu()
     finally:
         g.set_option(gemm.GEMM_OPT_TC_TMA_STORE, 1)
+        g.set_option(gemm.GEMM_OPT_SPLIT_K, 0)
     assert torch.equal(C_tma.cpu(), C_thr)
     assert torch.isnan(big[:, N:].cpu()).all()
 
@@ -366,6 +368,7 @@ def test_cluster_pairs_match_oracle_and_single_cta(g, oracle_mod, cluster_mode, 
     from dense_gemm_sm100_gb300 import gemm
     M, N, K = shape
     A, B = inp.make_operands(M, N, K, layout_b=layout, dist="normal", seed=M + 3 * N + K, dtype=mode)
+    g.set_option(gemm.GEMM_OPT_SPLIT_K, 1)  # these small shapes would otherwise be cut along K
     g.set_option(gemm.GEMM_OPT_TC_CLUSTER, 1)
     C1 = run_gpu(g, A, B, layout, mode).cpu()
     assert "cluster2" not in g.last_path and "pair" not in g.last_path
@@ -383,6 +386,7 @@ def test_cluster_pairs_match_oracle_and_single_cta(g, oracle_mod, cluster_mode, 
         assert ("+b3d" in g.last_path) == (layout == ROW and N % chunk == 0), g.last_path
     finally:
         g.set_option(gemm.GEMM_OPT_TC_CLUSTER, 3)
+        g.set_option(gemm.GEMM_OPT_SPLIT_K, 0)
     Cr, S = oracle_of(oracle_mod, A, B, layout)
     assert_parity(C2, Cr, S, TOL[mode], f"cluster mode {cluster_mode} {mode} {shape}")
     assert torch.equal(C1, C2)
@@ -483,6 +487,52 @@ def test_tail_tiles_split_along_k(g, oracle_mod, config, layout, M):
     assert_parity(C1, Cr, S, TOL["f32"], f"tail split config {config}")
     Cri, _ = oracle_of(oracle_mod, Ai, Bi, layout)
     assert np.array_equal(to_f64(Ci), Cri)
+
+
+@pytest.mark.parametrize("mode", ["tf32", "bf16"])
+@pytest.mark.parametrize("layout", [ROW, COL])
+@pytest.mark.parametrize("cluster_mode,shape,splits", [
+    (1, (128, 600, 700), 3),     # one CTA per tile, ragged N and K
+    (3, (300, 520, 640), 2),     # pair MMA, 3 tile rows: the odd CTA of the last pair is past M
+    (3, (640, 512, 1000), 5),
+])
+def test_tc_split_k_forced(g, oracle_mod, mode, layout, cluster_mode, shape, splits):
+    """Tensor-core K split: each tile unit in `splits` K slices whose partial
+    tiles a second kernel adds in slice order.  Same tolerance,
+    deterministic, exact on integer inputs."""
+    from dense_gemm_sm100_gb300 import gemm
+    M, N, K = shape
+    g.set_option(gemm.GEMM_OPT_TC_CLUSTER, cluster_mode)
+    g.set_option(gemm.GEMM_OPT_SPLIT_K, splits)
+    try:
+        A, B = inp.make_operands(M, N, K, layout_b=layout, dist="normal", seed=M + N + splits, dtype=mode)
+        C1 = run_gpu(g, A, B, layout, mode).cpu()
+        stages = -(-K // (64 if mode == "bf16" else 32))  # 128-byte K stages
+        per = -(-stages // splits)
+        assert f"+splitk{-(-stages // per)}" in g.last_path, g.last_path  # no empty slice
+        C2 = run_gpu(g, A, B, layout, mode).cpu()
+        Ai, Bi = inp.make_integer_operands(M, N, K, layout_b=layout, seed=splits, dtype=mode)
+        Ci = run_gpu(g, Ai, Bi, layout, mode)
+    finally:
+        g.set_option(gemm.GEMM_OPT_SPLIT_K, 0)
+        g.set_option(gemm.GEMM_OPT_TC_CLUSTER, 3)
+    assert torch.equal(C1, C2)
+    Cr, S = oracle_of(oracle_mod, A, B, layout)
+    assert_parity(C1, Cr, S, TOL[mode], f"tc split {splits} {mode} {shape}")
+    Cri, _ = oracle_of(oracle_mod, Ai, Bi, layout)
+    assert np.array_equal(to_f64(Ci), Cri)
+
+
+@pytest.mark.parametrize("mode", ["tf32", "bf16"])
+def test_tc_split_k_chosen_for_underfilled_shape(g, oracle_mod, mode):
+    """128 x 2048 is 8 tiles of 128x256 on 152 SMs: the K split is chosen
+    (a third of a wave or less)."""
+    M, N, K = 128, 2048, 1024
+    A, B = inp.make_operands(M, N, K, dist="normal", seed=9, dtype=mode)
+    C = run_gpu(g, A, B, ROW, mode)
+    assert "+splitk" in g.last_path, g.last_path
+    Cr, S = oracle_of(oracle_mod, A, B, ROW)
+    assert_parity(C, Cr, S, TOL[mode], f"tc chosen split {mode}")
 
 
 # ------------------------------------------------------- the five workloads
