@@ -29,6 +29,7 @@ struct gemm_ctx {
     int tc_group_m = 0;
     int max_ctas = 0;
     int simt_config = 0;  // 0: chosen per shape; else configuration index + 1
+    int elementwise = 0;  // FP32 unaligned operands: element-wise producer (1) or re-pack (0)
     int split_k = 0;      // 0: chosen per shape; 1: never; n > 1: n K slices (FP32 path)
     int tc_cluster = 3;   // tensor-core mode: 1 one CTA per tile, 2 multicast pairs, 3 pair MMA
     int tc_tma_store = 1; // tensor-core epilogue writes C with TMA stores when C allows it
@@ -115,6 +116,7 @@ bool tma_ready(const void *p, int64_t ld, int es)
 // the split-K partial products of the FP32 path.
 struct PackPlan {
     bool a = false, b = false;
+    bool elementwise = false;  // FP32, row-major B: copy unaligned operands element-wise instead
     int64_t lda = 0, ldb = 0;
     size_t a_bytes = 0, b_bytes = 0;
     int simt_config = 0;
@@ -137,6 +139,11 @@ PackPlan plan_pack(const gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_
     const int64_t align_elems = 16 / es;
     pp.a = h->force_repack || !tma_ready(A, lda, es);
     pp.b = h->force_repack || !tma_ready(B, ldb, es);
+    if (dtype == GEMM_F32 && layout_b == GEMM_B_ROW_MAJOR && !h->force_repack && h->elementwise &&
+        (pp.a || pp.b)) {
+        pp.elementwise = true;  // the producer reads A and B where they are
+        pp.a = pp.b = false;
+    }
     if (pp.a) {
         pp.lda = round_up(K, align_elems);
         pp.a_bytes = static_cast<size_t>(round_up(M * pp.lda * es, 256));
@@ -310,23 +317,30 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
     if (dtype == GEMM_F32) {
         const int cfg = pp.simt_config;
         const dg::SimtTile t = dg::simt_tile(cfg, layout_b);
-        rc = encode_2d(h, &tmA, 4, A, K, M, lda, dg::kSimtBK, t.bm);
-        if (rc) return rc;
-        if (layout_b == GEMM_B_ROW_MAJOR)
-            rc = encode_2d(h, &tmB, 4, B, N, K, ldb, 32, dg::kSimtBK);
-        else
-            rc = encode_2d(h, &tmB, 4, B, K, N, ldb, dg::kSimtBK, t.bn);
-        if (rc) return rc;
+        if (!pp.elementwise) {
+            rc = encode_2d(h, &tmA, 4, A, K, M, lda, dg::kSimtBK, t.bm);
+            if (rc) return rc;
+            if (layout_b == GEMM_B_ROW_MAJOR)
+                rc = encode_2d(h, &tmB, 4, B, N, K, ldb, 32, dg::kSimtBK);
+            else
+                rc = encode_2d(h, &tmB, 4, B, K, N, ldb, dg::kSimtBK, t.bn);
+            if (rc) return rc;
+        }
         dg::SplitK sk = pp.split;
         if (sk.splits > 1) sk.partials = reinterpret_cast<float *>(ws + pp.a_bytes + pp.b_bytes);
         const int64_t units = dg::simt_units(cfg, layout_b, M, N, sk);
         const int64_t cap = h->max_ctas > 0 ? h->max_ctas : int64_t{h->sm_count} * t.ctas_per_sm;
         lc.grid = static_cast<int>(units < cap ? units : cap);
         lc.group_m = h->simt_group_m;
-        cudaError_t e = dg::launch_simt_f32(cfg, tmA, tmB, layout_b, static_cast<int>(M), static_cast<int>(N),
-                                            static_cast<int>(K), C, ldc, c_vec4, lc, sk);
+        cudaError_t e =
+            pp.elementwise
+                ? dg::launch_simt_f32_elementwise(cfg, static_cast<const float *>(A), lda, static_cast<const float *>(B),
+                                                  ldb, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), C,
+                                                  ldc, c_vec4, lc, sk)
+                : dg::launch_simt_f32(cfg, tmA, tmB, layout_b, static_cast<int>(M), static_cast<int>(N),
+                                      static_cast<int>(K), C, ldc, c_vec4, lc, sk);
         if (e != cudaSuccess) return cuda_fail(h, e, "FP32 SIMT kernel launch");
-        path = std::string("simt_f32_") + t.name + "_" + lay + path;
+        path = std::string("simt_f32_") + t.name + "_" + lay + (pp.elementwise ? "+cpasync" : "") + path;
         if (sk.splits > 1) {
             ++h->launches;
             e = dg::launch_simt_tail_reduce(cfg, layout_b, static_cast<int>(M), static_cast<int>(N),
@@ -785,6 +799,10 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value)
         if (value < 0 || value > dg::simt_num_configs()) break;
         if (value > 0 && !dg::simt_config_usable(static_cast<int>(value) - 1)) break;
         h->simt_config = static_cast<int>(value);
+        return GEMM_OK;
+    case GEMM_OPT_ELEMENTWISE:
+        if (value != 0 && value != 1) break;
+        h->elementwise = static_cast<int>(value);
         return GEMM_OK;
     case GEMM_OPT_DEBUG_DROP_LOAD:
         if (value != 0 && value != 1) break;

@@ -77,6 +77,11 @@ cudaError_t prepare_tc();
 cudaError_t launch_simt_f32(int config, const CUtensorMap &tmA, const CUtensorMap &tmB,
                             int layout_b, int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
                             const LaunchCommon &lc, const SplitK &sk = SplitK());
+// The same for row-major B without TMA: A (pitch lda) and B (pitch ldb) at
+// any 4-byte-aligned address and pitch, copied element by element.
+cudaError_t launch_simt_f32_elementwise(int config, const float *A, int64_t lda, const float *B, int64_t ldb, int M,
+                                        int N, int K, float *C, int64_t ldc, bool c_vec4, const LaunchCommon &lc,
+                                        const SplitK &sk = SplitK());
 cudaError_t launch_simt_tail_reduce(int config, int layout_b, int M, int N, int K, float *C, int64_t ldc,
                                     bool c_vec4, const LaunchCommon &lc, const SplitK &sk, int sm_count);
 

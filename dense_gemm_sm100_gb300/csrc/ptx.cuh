@@ -168,6 +168,25 @@ __device__ __forceinline__ void bulk_wait_group_all()
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// 4-byte asynchronous copy global -> shared; src_bytes = 0 writes zeros
+// (the source is not read).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued so far has landed;
+// the arrival is one of the barrier's expected count (no increment).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Makes generic-proxy shared-memory writes visible to the async proxy (TMA).
 __device__ __forceinline__ void fence_proxy_async_shared()
 {

@@ -29,6 +29,7 @@
 // Out-of-range elements of A and B are zero-filled by TMA; stores of C are
 // guarded, so any M, N, K works.
 #include <cstdint>
+#include <cstring>
 
 #include "gemm_internal.h"
 #include "ptx.cuh"
@@ -47,6 +48,9 @@ struct SimtParams {
     // go to `partials` (slice-major, BM x BN floats each).
     int full_units, tail_tiles, splits, k_per_split;
     float *partials;
+    // operands for the element-wise producer (LAYOUT_B == 3)
+    const float *A, *B;
+    long long lda, ldb;
     float *C;
     long long ldc;
     int *status;
@@ -114,7 +118,11 @@ __device__ __forceinline__ Unit unit_coords(int u, const SimtParams &p)
 // memory by the consumers; 2 = column-major B turned in shared memory by the
 // producer warp ("PMPP Chapter 06", section 1, corner turning): TMA lands the
 // K-contiguous tile, the warp rewrites it in the row-major staging layout,
-// and the consumers run the row-major (packed) inner loop.
+// and the consumers run the row-major (packed) inner loop; 3 = row-major B
+// with A or B at a pitch or address TMA cannot use (not a multiple of 16
+// bytes): the producer warps copy every element with a 4-byte cp.async
+// straight into the swizzled staging layout, zero-filling outside the
+// matrices ("GEMM 性能优化", 台阶 7, asynchronous copies).
 template <int LAYOUT_B, int WM, int WN, int TN, int STAGES, int GU, int F2, int PWG>
 struct Simt {
     static_assert(WM % 2 == 0, "row interleave pairs warps along M");
@@ -136,13 +144,16 @@ struct Simt {
     static constexpr int PRODUCER_WARPS = PWG ? 4 : 1;
     static constexpr int THREADS = (CONSUMER_WARPS + PRODUCER_WARPS) * 32;
     static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8;  // what __launch_bounds__ allows
-    // the corner turn (column-major B) needs a few more registers than the copies alone
-    static constexpr int PRODUCER_REGS = CONSUMER_WARPS > 8 ? (LAYOUT_B == 2 ? 32 : 24) : 40;
+    // the corner turn (column-major B) and the element-wise copies need more
+    // registers than issuing TMA copies alone
+    static constexpr int PRODUCER_REGS =
+        CONSUMER_WARPS > 8 ? (LAYOUT_B == 3 ? 40 : LAYOUT_B == 2 ? 32 : 24) : 40;
     static constexpr int CONSUMER_REGS =
         ((LAUNCH_REGS * THREADS - PRODUCER_REGS * PRODUCER_WARPS * 32) / (CONSUMER_WARPS * 32)) / 8 * 8 > 240
             ? 240
             : ((LAUNCH_REGS * THREADS - PRODUCER_REGS * PRODUCER_WARPS * 32) / (CONSUMER_WARPS * 32)) / 8 * 8;
     static_assert(!PWG || (CONSUMER_WARPS % 4 == 0 && LAYOUT_B != 1), "warpgroups; B read as row-major");
+    static_assert(LAYOUT_B != 3 || BN % 32 == 0, "element-wise B copies fill 32-column boxes");
     // 16 consumer warps leave 112 registers a thread: A fragments are then
     // loaded 2 k at a time (8-byte loads) instead of 4, to fit.
     static constexpr bool A_PAIRS = CONSUMER_WARPS >= 16;
@@ -165,7 +176,7 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
     const uint32_t pad = ((raw_addr + 1023u) & ~1023u) - raw_addr;
     uint8_t *smem = smem_raw + pad;
     const uint32_t sbase = raw_addr + pad;
-    constexpr int RL = LAYOUT_B == 2 ? 0 : LAYOUT_B;  // layout the consumers read
+    constexpr int RL = LAYOUT_B == 1 ? 1 : 0;  // layout the consumers read
     constexpr int LAND = A_BYTES + S::B_BYTES;        // landing zone offset (LAYOUT_B == 2)
     const uint32_t full_bar = sbase + STAGES * STAGE_BYTES;  // STAGES x 8 bytes
     const uint32_t empty_bar = full_bar + STAGES * 8;         // STAGES x 8 bytes
@@ -179,7 +190,9 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar + 8 * s, 1);
+            // TMA: one arrival plus the bytes; element-wise copies: one
+            // arrival per producer thread when its copies have landed
+            mbar_init(full_bar + 8 * s, LAYOUT_B == 3 ? S::PRODUCER_WARPS * 32 : 1);
             mbar_init(empty_bar + 8 * s, CONSUMER_WARPS);
             if (LAYOUT_B == 2) mbar_init(ready_bar + 8 * s, S::PRODUCER_WARPS);  // every turning warp
         }
@@ -192,11 +205,59 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
         if (warp >= CONSUMER_WARPS) {
             setmaxnreg_dec<S::PRODUCER_REGS>();
             // one warp of the group issues the copies; with column-major B
-            // all four share the corner turn
-            if (warp != CONSUMER_WARPS && LAYOUT_B != 2) return;
+            // all four share the corner turn, with element-wise copies all
+            // four copy
+            if (warp != CONSUMER_WARPS && LAYOUT_B != 2 && LAYOUT_B != 3) return;
         } else {
             setmaxnreg_inc<S::CONSUMER_REGS>();
         }
+    }
+
+    if (LAYOUT_B == 3 && warp >= CONSUMER_WARPS) {
+        // ------------------------------------------- element-wise producer
+        // Thread pt of the PT producer threads copies elements pt, pt + PT,
+        // ... of the stage: consecutive threads take consecutive k of an A
+        // row and consecutive columns of a B row (coalesced reads; each warp
+        // writes one 128-byte swizzled row, 32 distinct banks).
+        constexpr int PT = S::PRODUCER_WARPS * 32;
+        const int pt = threadIdx.x - CONSUMER_WARPS * 32;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int unit = blockIdx.x; ok && unit < num_units; unit += gridDim.x) {
+            const Unit w = unit_coords(unit, p);
+            for (int kt = w.kt_begin; kt < w.kt_end; ++kt, ++it) {
+                const uint32_t s = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1u;
+                bool got = true;
+                if (lane == 0)
+                    got = mbar_wait(empty_bar + 8 * s, ph ^ 1u, abort_flag, p.status, kWaitProducerEmpty,
+                                    p.timeout_ns);
+                if (__shfl_sync(0xffffffffu, got ? 1 : 0, 0) == 0) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t st = sbase + s * STAGE_BYTES;
+                const int k0 = kt * BK;
+                for (int e = pt; e < BM * BK; e += PT) {
+                    const int r = e / BK, kk = e - (e / BK) * BK;
+                    const long long m = (long long)w.mb * BM + r;
+                    const bool in = m < p.M && k0 + kk < p.K;
+                    const uint32_t dst = st + r * 128 + ((((kk >> 2) ^ (r & 7)) << 4) | ((kk & 3) << 2));
+                    cp_async_4(dst, in ? p.A + m * p.lda + k0 + kk : p.A, in ? 4u : 0u);
+                }
+                for (int e = pt; e < BK * BN; e += PT) {
+                    const int kk = e / BN, n = e - (e / BN) * BN;
+                    const long long col = (long long)w.nb * BN + n;
+                    const bool in = col < p.N && k0 + kk < p.K;
+                    const uint32_t dst = st + A_BYTES + (n >> 5) * 4096 + kk * 128 +
+                                         (((((n & 31) >> 2) ^ (kk & 7)) << 4) | ((n & 3) << 2));
+                    cp_async_4(dst, in ? p.B + (long long)(k0 + kk) * p.ldb + col : p.B, in ? 4u : 0u);
+                }
+                cp_async_mbar_arrive_noinc(full_bar + 8 * s);
+            }
+        }
+        cp_async_wait_all();  // no copy lands after the CTA has gone
+        return;
     }
 
     if (LAYOUT_B == 2 && warp >= CONSUMER_WARPS) {
@@ -607,12 +668,14 @@ constexpr int col_pwg(int wn, int tn, int f2, int pwg) { return pwg && col_layou
 template <int WM, int WN, int TN, int ST, int GU, int F2, int PWG>
 cudaError_t prepare_cfg(int *ctas)
 {
-    int c0 = 0, c1 = 0;
+    int c0 = 0, c1 = 0, c3 = 0;
     cudaError_t e = prepare_one<0, WM, WN, TN, ST, GU, F2, PWG>(&c0);
     if (e == cudaSuccess)
         e = prepare_one<col_layout(WN, TN, F2), WM, WN, col_tn(TN), col_stages(WM, WN, TN, F2, ST), GU, F2,
                         col_pwg(WN, TN, F2, PWG)>(&c1);
+    if (e == cudaSuccess) e = prepare_one<3, WM, WN, TN, ST, GU, F2, PWG>(&c3);
     *ctas = c0 < c1 ? c0 : c1;
+    *ctas = *ctas < c3 ? *ctas : c3;
     return e;
 }
 
@@ -623,6 +686,9 @@ void launch_cfg(int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB, co
     if (layout_b == 0) {
         using S = Simt<0, WM, WN, TN, ST, GU, F2, PWG>;
         sgemm_simt_kernel<0, WM, WN, TN, ST, GU, F2, PWG><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
+    } else if (layout_b == 3) {
+        using S = Simt<3, WM, WN, TN, ST, GU, F2, PWG>;
+        sgemm_simt_kernel<3, WM, WN, TN, ST, GU, F2, PWG><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
     } else {
         constexpr int L = col_layout(WN, TN, F2), CST = col_stages(WM, WN, TN, F2, ST);
         constexpr int CP = col_pwg(WN, TN, F2, PWG);
@@ -789,6 +855,10 @@ SimtParams simt_params(int config, int layout_b, int M, int N, int K, float *C, 
     p.timeout_ns = lc.timeout_ns;
     p.c_vec4 = c_vec4 ? 1 : 0;
     p.debug_drop = lc.debug_drop;
+    p.A = nullptr;
+    p.B = nullptr;
+    p.lda = 0;
+    p.ldb = 0;
     return p;
 }
 
@@ -814,6 +884,21 @@ cudaError_t launch_simt_f32(int config, const CUtensorMap &tmA, const CUtensorMa
 {
     const SimtParams p = simt_params(config, layout_b, M, N, K, C, ldc, c_vec4, lc, sk);
     g_configs[config].launch(layout_b, tmA, tmB, p, lc.grid, lc.stream);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_simt_f32_elementwise(int config, const float *A, int64_t lda, const float *B, int64_t ldb, int M,
+                                        int N, int K, float *C, int64_t ldc, bool c_vec4, const LaunchCommon &lc,
+                                        const SplitK &sk)
+{
+    SimtParams p = simt_params(config, 0, M, N, K, C, ldc, c_vec4, lc, sk);
+    p.A = A;
+    p.B = B;
+    p.lda = lda;
+    p.ldb = ldb;
+    CUtensorMap unused;
+    memset(&unused, 0, sizeof unused);
+    g_configs[config].launch(3, unused, unused, p, lc.grid, lc.stream);
     return cudaGetLastError();
 }
 

@@ -101,6 +101,13 @@ extern "C" {
  * GEMM_OPT_WAIT_TIMEOUT_NS; the kernel then leaves C incomplete, ends, and
  * gemm_sync_status reports GEMM_ERR_TIMEOUT.  The context stays usable. */
 #define GEMM_OPT_DEBUG_DROP_LOAD 10
+/* FP32 with row-major B and an operand TMA cannot address (base or pitch not
+ * a multiple of 16 bytes): 0 (default) = re-pack the operand into the
+ * workspace first, then TMA; 1 = the producer warps copy A and B element by
+ * element with 4-byte cp.async into the shared-memory ring (no workspace for
+ * the operands, but 2-4x slower: the copies cannot keep the ring fed).
+ * Tensor-core modes and column-major B always re-pack. */
+#define GEMM_OPT_ELEMENTWISE 11
 
 typedef struct gemm_ctx *gemm_handle_t;
 

@@ -131,7 +131,11 @@ def test_blocked_matrix_identity(g, oracle_mod, mode, layout):
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("layout", [ROW, COL])
 def test_unaligned_leading_dimensions(g, oracle_mod, mode, layout):
-    """Odd leading dimensions and an offset base pointer (re-pack path)."""
+    """Odd leading dimensions and an offset base pointer, which TMA cannot
+    address: re-packed first; FP32 with row-major B can instead copy them
+    element by element into the shared-memory ring (cp.async,
+    GEMM_OPT_ELEMENTWISE = 1).  Same bits either way."""
+    from dense_gemm_sm100_gb300 import gemm
     M, N, K = 97, 203, 151
     A, B = inp.make_operands(M, N, K, layout_b=layout, seed=23, dist="normal", dtype=mode)
     dev = torch.device("cuda", 0)
@@ -145,6 +149,16 @@ def test_unaligned_leading_dimensions(g, oracle_mod, mode, layout):
     g.run(Ap[:, 1:K + 1], Bp[:, 1:cols_b + 1], C, layout, mode)
     g.sync_status()
     assert "repackA" in g.last_path and "repackB" in g.last_path
+    if mode == "f32" and layout == ROW:
+        C_first = C.clone()
+        g.set_option(gemm.GEMM_OPT_ELEMENTWISE, 1)
+        try:
+            g.run(Ap[:, 1:K + 1], Bp[:, 1:cols_b + 1], C, layout, mode)
+            g.sync_status()
+            assert "+cpasync" in g.last_path and "repack" not in g.last_path, g.last_path
+        finally:
+            g.set_option(gemm.GEMM_OPT_ELEMENTWISE, 0)
+        assert torch.equal(C_first, C)
     Cr, S = oracle_of(oracle_mod, A, B, layout)
     assert_parity(C, Cr, S, TOL[mode])
 
@@ -560,14 +574,24 @@ def test_workload_full(g, oracle_mod, name):
     assert_parity(C, Cr, S, TOL[w.dtype], name)
 
 
-def test_workload_ragged_4095x3073x2047(g, oracle_mod):
+@pytest.mark.parametrize("elementwise", [1, 0])
+def test_workload_ragged_4095x3073x2047(g, oracle_mod, elementwise):
     """Non-tile-multiple edges with tight (not 16-byte multiple) leading
-    dimensions: checked on every row in a band at each edge and a sample of
-    the interior."""
+    dimensions, through the element-wise producer and through re-packing:
+    checked on every row in a band at each edge and a sample of the
+    interior."""
+    from dense_gemm_sm100_gb300 import gemm
     w = inp.WORKLOADS["fp32_4095x3073x2047_row"]
     A, B = inp.make_workload(w)
-    C = run_gpu(g, A, B, w.layout_b, w.dtype)
-    assert "repackA" in g.last_path and "repackB" in g.last_path
+    g.set_option(gemm.GEMM_OPT_ELEMENTWISE, elementwise)
+    try:
+        C = run_gpu(g, A, B, w.layout_b, w.dtype)
+    finally:
+        g.set_option(gemm.GEMM_OPT_ELEMENTWISE, 0)
+    if elementwise:
+        assert "+cpasync" in g.last_path, g.last_path
+    else:
+        assert "repackA" in g.last_path and "repackB" in g.last_path
     rows = sorted(set(range(0, 130)) | set(range(w.M - 130, w.M)) |
                   set(inp.sample_indices(w.M, 64, seed=7)))
     cols = sorted(set(range(0, 260)) | set(range(w.N - 260, w.N)) |

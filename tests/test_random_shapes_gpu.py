@@ -31,8 +31,9 @@ def cases():
         tc_mode = rng.choice([1, 2, 3, 3]) if mode != "f32" else 3
         max_ctas = rng.choice([0, 0, 4, 8, 16])
         integer = rng.random() < 0.3
+        elementwise = 1 if (mode == "f32" and layout == inp.B_ROW_MAJOR and rng.random() < 0.3) else 0
         host = rng.random() < 0.2  # through gemm_run_host (pinned host buffers)
-        out.append((i, mode, layout, (M, N, K), simt_config, tc_mode, max_ctas, integer, host))
+        out.append((i, mode, layout, (M, N, K), simt_config, tc_mode, max_ctas, integer, host, elementwise))
     return out
 
 
@@ -50,7 +51,7 @@ def g():
 @pytest.mark.parametrize("case", cases(), ids=lambda c: f"case{c[0]}")
 def test_random_shape(g, oracle_mod, case):
     from dense_gemm_sm100_gb300 import gemm
-    _, mode, layout, (M, N, K), simt_config, tc_mode, max_ctas, integer, host = case
+    _, mode, layout, (M, N, K), simt_config, tc_mode, max_ctas, integer, host, elementwise = case
     if integer:
         A, B = inp.make_integer_operands(M, N, K, layout_b=layout, seed=M * 7 + N, dtype=mode)
     else:
@@ -58,6 +59,7 @@ def test_random_shape(g, oracle_mod, case):
     g.set_option(gemm.GEMM_OPT_SIMT_CONFIG, simt_config)
     g.set_option(gemm.GEMM_OPT_TC_CLUSTER, tc_mode)
     g.set_option(gemm.GEMM_OPT_MAX_CTAS, max_ctas)
+    g.set_option(gemm.GEMM_OPT_ELEMENTWISE, elementwise)
     try:
         if host:
             C = torch.full((M, N), float("nan")).pin_memory()
@@ -73,6 +75,7 @@ def test_random_shape(g, oracle_mod, case):
         g.set_option(gemm.GEMM_OPT_SIMT_CONFIG, 0)
         g.set_option(gemm.GEMM_OPT_TC_CLUSTER, 3)
         g.set_option(gemm.GEMM_OPT_MAX_CTAS, 0)
+        g.set_option(gemm.GEMM_OPT_ELEMENTWISE, 0)
     Cr, S = oracle_mod.gemm(to_f64(A), to_f64(B), layout)
     if integer:
         assert np.array_equal(to_f64(C), Cr), path
