@@ -367,6 +367,16 @@ PAGES_LADDER_PCT = {1: (6, 11), 2: (25, 40), 3: (50, 65), 4: (60, 75), 5: (70, 8
                     6: (80, 87), 7: (90, 97)}
 
 
+def apply_options(g, args):
+    from dense_gemm_sm100_gb300 import gemm
+    if args.simt_config:
+        g.set_option(gemm.GEMM_OPT_SIMT_CONFIG, args.simt_config)
+    if args.tc_mode:
+        g.set_option(gemm.GEMM_OPT_TC_CLUSTER, args.tc_mode)
+    if args.split_k:
+        g.set_option(gemm.GEMM_OPT_SPLIT_K, args.split_k)
+
+
 def run_configs(args):
     """Every workload of the specification, timed two ways: warm (back-to-back
     steps) and with the L2 scrubbed before each step (a 2 x L2 buffer written
@@ -382,8 +392,19 @@ def run_configs(args):
     steps = max(5, min(args.steps, 30))
     scrub = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
     g = gemm.Gemm(0)
+    apply_options(g, args)
+    done = {}
+    if args.results and os.path.exists(args.results):
+        for line in open(args.results):
+            if line.strip():
+                r = json.loads(line)
+                done[r["workload"]] = r
     out = []
+    small_c = {}
     for name, w in inp.WORKLOADS.items():
+        if name in done:  # resume: measured by an earlier run
+            out.append(done[name])
+            continue
         A, B = inp.make_workload(w)
         A_d, B_d = A.to(dev), B.to(dev)
         C_d = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
@@ -405,6 +426,8 @@ def run_configs(args):
             e1.synchronize()
             cold.append(e0.elapsed_time(e1))
         g.sync_status(stream)
+        if name in ("fp32_128_row", "fp32_1024_colB"):
+            small_c[name] = C_d.double().cpu().numpy()
         # labelled side reference: cuBLAS through torch on the same operands
         torch.backends.cuda.matmul.allow_tf32 = w.dtype == "tf32"
         Bl = B_d if w.layout_b == 0 else B_d.t()
@@ -422,6 +445,9 @@ def run_configs(args):
                                     "what": "torch.matmul (cuBLAS), warm, " +
                                             ("BF16 output" if w.dtype == "bf16" else
                                              "TF32 allowed" if w.dtype == "tf32" else "TF32 off")}})
+        if args.results:
+            with open(args.results, "a") as f:
+                f.write(json.dumps(out[-1]) + "\n")
         del A_d, B_d, C_d
         torch.cuda.empty_cache()
     g.close()
@@ -432,10 +458,15 @@ def run_configs(args):
         A64, B64 = A.double().numpy(), B.double().numpy()
         for threads in (1, oracle.default_threads()):
             t = time.perf_counter()
-            oracle.gemm(A64, B64, w.layout_b, nthreads=threads)
+            Cr, S = oracle.gemm(A64, B64, w.layout_b, nthreads=threads)
             dt = time.perf_counter() - t
-            cpu.append({"workload": name, "threads": threads, "seconds": round(dt, 4),
-                        "gflops": round(w.flops / dt / 1e9, 3)})
+            entry = {"workload": name, "threads": threads, "seconds": round(dt, 4),
+                     "gflops": round(w.flops / dt / 1e9, 3)}
+            if name in small_c:  # this run's GPU result against the oracle
+                import numpy as np
+                err = np.abs(small_c[name] - Cr) / np.maximum(S, 1e-300)
+                entry["gpu_max_err_over_sum_abs"] = float(err.max())
+            cpu.append(entry)
     print(json.dumps({"configs": out, "oracle": cpu}))
     return 0
 
@@ -537,6 +568,15 @@ def main(argv=None):
                     help="skip the labelled cuBLAS side reference")
     ap.add_argument("--ladder", action="store_true",
                     help="time the labelled ladder suite (pages' optimisation steps) instead")
+    ap.add_argument("--simt-config", type=int, default=0,
+                    help="force the FP32 tile configuration (GEMM_OPT_SIMT_CONFIG; 0 = chosen per shape)")
+    ap.add_argument("--tc-mode", type=int, default=0,
+                    help="force the tensor-core mode (GEMM_OPT_TC_CLUSTER 1..3; 0 = default)")
+    ap.add_argument("--split-k", type=int, default=0,
+                    help="GEMM_OPT_SPLIT_K (0 = chosen per shape, 1 = never, n = n slices)")
+    ap.add_argument("--results", default=None,
+                    help="with --configs: append one JSON line per finished workload to this file "
+                         "and skip workloads already in it")
     ap.add_argument("--configs", action="store_true",
                     help="time every specified workload warm and with L2 scrubbed, and the oracle "
                          "on the small ones with 1 and all host threads (one JSON document)")
@@ -562,6 +602,7 @@ def main(argv=None):
     torch.cuda.set_device(dev_index)
     peaks, peak_note = load_peaks()
     g = gemm.Gemm(dev_index)
+    apply_options(g, args)
     rank0 = ctx is None or ctx["rank"] == 0
 
     sampler = ClockSampler(dev_index) if rank0 else None

@@ -30,6 +30,7 @@ struct gemm_ctx {
     int max_ctas = 0;
     int simt_config = 0;  // 0: chosen per shape; else configuration index + 1
     int elementwise = 0;  // FP32 unaligned operands: element-wise producer (1) or re-pack (0)
+    size_t ws_limit = 0;  // 0: none; else the workspace never grows beyond this many bytes
     int split_k = 0;      // 0: chosen per shape; 1: never; n > 1: n K slices (FP32 path)
     int tc_cluster = 3;   // tensor-core mode: 1 one CTA per tile, 2 multicast pairs, 3 pair MMA
     int tc_tma_store = 1; // tensor-core epilogue writes C with TMA stores when C allows it
@@ -182,9 +183,16 @@ PackPlan plan_pack(const gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_
 int ensure_workspace(gemm_ctx *h, size_t need)
 {
     if (need <= h->ws_bytes) return GEMM_OK;
+    if (h->ws_limit > 0 && need > h->ws_limit) {
+        char msg[160];
+        std::snprintf(msg, sizeof msg, "workspace of %zu bytes needed, limit %zu (GEMM_OPT_WORKSPACE_LIMIT)", need,
+                      h->ws_limit);
+        return fail(h, GEMM_ERR_NOMEM, msg);
+    }
     size_t grow = h->ws_bytes + h->ws_bytes / 2;
     size_t bytes = need > grow ? need : grow;
     bytes = (bytes + (size_t{2} << 20) - 1) & ~((size_t{2} << 20) - 1);
+    if (h->ws_limit > 0 && bytes > h->ws_limit) bytes = need;  // stay within the limit
     // Earlier queued work may still read the old buffer.
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(h, e, "cudaDeviceSynchronize before workspace growth");
@@ -799,6 +807,10 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value)
         if (value < 0 || value > dg::simt_num_configs()) break;
         if (value > 0 && !dg::simt_config_usable(static_cast<int>(value) - 1)) break;
         h->simt_config = static_cast<int>(value);
+        return GEMM_OK;
+    case GEMM_OPT_WORKSPACE_LIMIT:
+        if (value < 0) break;
+        h->ws_limit = static_cast<size_t>(value);
         return GEMM_OK;
     case GEMM_OPT_ELEMENTWISE:
         if (value != 0 && value != 1) break;

@@ -108,6 +108,11 @@ extern "C" {
  * the operands, but 2-4x slower: the copies cannot keep the ring fed).
  * Tensor-core modes and column-major B always re-pack. */
 #define GEMM_OPT_ELEMENTWISE 11
+/* Cap on the handle's workspace in bytes (0 = none, the default).  A run
+ * that would need more (re-packed operands, split-K partial tiles, staged
+ * host buffers) fails with GEMM_ERR_NOMEM before launching anything; an
+ * allocation already made is kept. */
+#define GEMM_OPT_WORKSPACE_LIMIT 12
 
 typedef struct gemm_ctx *gemm_handle_t;
 

@@ -356,6 +356,41 @@ def test_run_host_orders_with_the_callers_stream(g, oracle_mod):
         g.set_option(gemm.GEMM_OPT_MAX_CTAS, 0)
 
 
+def test_workspace_limit_reports_nomem_without_launching(g, oracle_mod):
+    """An allocation failure injected on the host: with the workspace capped,
+    a run that needs to re-pack its operands returns GEMM_ERR_NOMEM before
+    any launch, C stays untouched, and the handle works again once the cap
+    is lifted."""
+    from dense_gemm_sm100_gb300 import gemm
+    M, N, K = 300, 257, 131  # K and N odd: both operands need a re-pack
+    A, B = inp.make_integer_operands(M, N, K, seed=3)
+    dev = torch.device("cuda", 0)
+    A_d, B_d = A.to(dev), B.to(dev)
+    C = torch.full((M, N), -7.0, device=dev)
+    g.sync_status()
+    before = g.launch_count
+    g.set_option(gemm.GEMM_OPT_WORKSPACE_LIMIT, 4096)
+    try:
+        h = gemm.Gemm(0)  # a fresh handle has no workspace yet
+        h.set_option(gemm.GEMM_OPT_WORKSPACE_LIMIT, 4096)
+        with pytest.raises(gemm.GemmError) as err:
+            h.run(A_d, B_d, C, ROW, "f32")
+        assert err.value.code == gemm.GEMM_ERR_NOMEM
+        assert "GEMM_OPT_WORKSPACE_LIMIT" in gemm.gemm_last_error_string(h.handle)
+        assert h.launch_count == 0
+        torch.cuda.synchronize()
+        assert torch.all(C == -7.0)
+        h.set_option(gemm.GEMM_OPT_WORKSPACE_LIMIT, 0)
+        h.run(A_d, B_d, C, ROW, "f32")
+        h.sync_status()
+        h.close()
+    finally:
+        g.set_option(gemm.GEMM_OPT_WORKSPACE_LIMIT, 0)
+    assert g.launch_count == before
+    Cr, _ = oracle_of(oracle_mod, A, B, ROW)
+    assert np.array_equal(to_f64(C), Cr)
+
+
 def test_launch_count_increments(g):
     before = g.launch_count
     A, B = inp.make_operands(64, 64, 64, seed=1)
