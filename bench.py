@@ -367,6 +367,69 @@ PAGES_LADDER_PCT = {1: (6, 11), 2: (25, 40), 3: (50, 65), 4: (60, 75), 5: (70, 8
                     6: (80, 87), 7: (90, 97)}
 
 
+NCU_SUMMARY_METRICS = [
+    ("duration", "gpu__time_duration.sum"),
+    ("SM clock", "sm__cycles_elapsed.avg.per_second"),
+    ("FMA pipe busy (% of active)", "sm__pipe_fma_cycles_active.avg.pct_of_peak_sustained_active"),
+    ("tensor pipe busy (% of active)", "sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_active"),
+    ("issue active (%)", "smsp__issue_active.avg.pct_of_peak_sustained_active"),
+    ("DRAM read", "dram__bytes_read.sum"),
+    ("DRAM write", "dram__bytes_write.sum"),
+    ("L2 hit rate", "lts__t_sector_hit_rate.pct"),
+    ("L2 -> SM bytes", "l1tex__m_xbar2l1tex_read_bytes.sum"),
+    ("shared-load bank conflicts", "l1tex__data_bank_conflicts_pipe_lsu_mem_shared_op_ld.sum"),
+    ("registers / thread", "launch__registers_per_thread"),
+    ("warps active (% of peak)", "sm__warps_active.avg.pct_of_peak_sustained_active"),
+    ("grid", "launch__grid_size"),
+    ("block", "launch__block_size"),
+    ("dynamic shared memory", "launch__shared_mem_per_block_dynamic"),
+]
+STALL_PREFIX = "smsp__average_warps_issue_stalled_"
+STALL_SUFFIX = "_per_issue_active.ratio"
+
+
+def ncu_summary_markdown(csv_text: str, top_stalls: int = 5) -> str:
+    """Markdown table of the usual metrics, one column per captured launch,
+    from `ncu -i REPORT --page raw --csv` output (rows: header, units, one
+    row per launch).  Metrics the report lacks are skipped."""
+    import csv
+    import io
+    rows = [r for r in csv.reader(io.StringIO(csv_text)) if r]
+    head, units, launches = rows[0], rows[1], rows[2:]
+    col = {name: i for i, name in enumerate(head)}
+    names = [r[col["Kernel Name"]][:60] if "Kernel Name" in col else f"launch {j}"
+             for j, r in enumerate(launches)]
+    out = ["| metric | " + " | ".join(f"`{n}`" for n in names) + " |",
+           "|---|" + "---|" * len(launches)]
+    for label, metric in NCU_SUMMARY_METRICS:
+        if metric in col:
+            i = col[metric]
+            out.append(f"| {label} | " + " | ".join(f"{r[i]} {units[i]}".strip() for r in launches) + " |")
+    stalls = [(name[len(STALL_PREFIX):-len(STALL_SUFFIX)], i) for name, i in col.items()
+              if name.startswith(STALL_PREFIX) and name.endswith(STALL_SUFFIX)]
+    for j, r in enumerate(launches):
+        vals = []
+        for stall, i in stalls:
+            try:
+                vals.append((float(r[i].replace(",", "")), stall))
+            except ValueError:
+                pass
+        vals.sort(reverse=True)
+        top = ", ".join(f"{s} {v:.2f}" for v, s in vals[:top_stalls])
+        out.append(f"| top stalls per issued instruction ({names[j]}) | {top} |" + " |" * (len(launches) - 1))
+    return "\n".join(out) + "\n"
+
+
+def run_ncu_summary(path):
+    import subprocess
+    r = subprocess.run(["ncu", "-i", path, "--page", "raw", "--csv"], capture_output=True, text=True)
+    if r.returncode != 0:
+        print(r.stderr, file=sys.stderr)
+        return r.returncode
+    print(ncu_summary_markdown(r.stdout), end="")
+    return 0
+
+
 def apply_options(g, args):
     from dense_gemm_sm100_gb300 import gemm
     if args.simt_config:
@@ -577,6 +640,8 @@ def main(argv=None):
     ap.add_argument("--results", default=None,
                     help="with --configs: append one JSON line per finished workload to this file "
                          "and skip workloads already in it")
+    ap.add_argument("--ncu-summary", default=None, metavar="REPORT",
+                    help="print a Markdown table of the usual metrics from an ncu report (no GPU needed)")
     ap.add_argument("--configs", action="store_true",
                     help="time every specified workload warm and with L2 scrubbed, and the oracle "
                          "on the small ones with 1 and all host threads (one JSON document)")
@@ -588,6 +653,8 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
+    if args.ncu_summary:
+        return run_ncu_summary(args.ncu_summary)
     ctx = dist_setup()
     if args.impl == "reference":
         return run_reference(args, ctx)

@@ -76,3 +76,24 @@ def test_clock_summary_filters_window(tmp_path):
     t0 = time.mktime(time.strptime("2026/12/02 10:00:01", "%Y/%m/%d %H:%M:%S"))
     out = s.summary(t0, t0 + 1.0)
     assert out["samples"] == 2 and out["sm_mhz"] == 1925 and out["reasons"] == ["sw_power_cap"]
+
+
+def test_ncu_summary_table_from_raw_csv():
+    """The ncu summary turns `ncu -i ... --page raw --csv` text into a
+    Markdown table: labelled metrics with units, missing metrics skipped,
+    stall reasons sorted by their per-instruction weight."""
+    import bench
+    csv_text = (
+        '"ID","Kernel Name","gpu__time_duration.sum","sm__pipe_fma_cycles_active.avg.pct_of_peak_sustained_active",'
+        '"launch__registers_per_thread","smsp__average_warps_issue_stalled_wait_per_issue_active.ratio",'
+        '"smsp__average_warps_issue_stalled_math_pipe_throttle_per_issue_active.ratio"\n'
+        '"","","ms","%","register/thread","inst","inst"\n'
+        '"0","sgemm_simt_kernel","1.83","83.6","128","1.13","2.10"\n')
+    md = bench.ncu_summary_markdown(csv_text)
+    lines = md.splitlines()
+    assert lines[0] == "| metric | `sgemm_simt_kernel` |"
+    assert "| duration | 1.83 ms |" in lines
+    assert "| FMA pipe busy (% of active) | 83.6 % |" in lines
+    assert "| registers / thread | 128 register/thread |" in lines
+    assert not any(l.startswith("| tensor pipe") for l in lines)  # not in the report
+    assert lines[-1].startswith("| top stalls per issued instruction (sgemm_simt_kernel) | math_pipe_throttle 2.10, wait 1.13")
