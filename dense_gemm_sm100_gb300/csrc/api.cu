@@ -34,6 +34,7 @@ struct gemm_ctx {
     int split_k = 0;      // 0: chosen per shape; 1: never; n > 1: n K slices (FP32 path)
     int tc_cluster = 3;   // tensor-core mode: 1 one CTA per tile, 2 multicast pairs, 3 pair MMA
     int tc_tma_store = 1; // tensor-core epilogue writes C with TMA stores when C allows it
+    int tc_slices = 0;    // pair MMA: K slices per ring stage (0: library's choice)
     int debug_drop = 0;   // test hook (GEMM_OPT_DEBUG_DROP_LOAD)
     // gemm_run_host pipeline: copy streams and events (created on first use)
     cudaStream_t copy_in = nullptr, copy_out = nullptr;
@@ -385,12 +386,14 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
             rc = encode_2d(h, &tmC, 4, C, N, M, ldc, dg::kTcBoxC, dg::kTcBoxC);
             if (rc) return rc;
         }
+        const bool wide = cluster == 3 && sp.splits == 1 && h->tc_slices == 2;
         cudaError_t e = dg::launch_tc(dtype, layout_b, tmA, tmB, c_tma ? &tmC : nullptr, static_cast<int>(M),
                                       static_cast<int>(N), static_cast<int>(K), C, ldc, c_vec4, lc, cluster,
-                                      b_chunks, sp);
+                                      b_chunks, sp, wide);
         if (e != cudaSuccess) return cuda_fail(h, e, "tensor-core kernel launch");
         path = std::string(dtype == GEMM_BF16 ? "tc_bf16" : "tc_tf32") +
-               (cluster == 3 ? "_pair256x256_" : "_128x256_") + lay + (cluster == 2 ? "_cluster2" : "") +
+               (cluster == 3 ? (wide ? "_pair256x256w_" : "_pair256x256_") : "_128x256_") + lay +
+               (cluster == 2 ? "_cluster2" : "") +
                (b_chunks ? "+b3d" : "") + path;
         if (sp.splits > 1) {
             ++h->launches;
@@ -827,6 +830,10 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value)
     case GEMM_OPT_TC_CLUSTER:
         if (value < 1 || value > 3) break;
         h->tc_cluster = static_cast<int>(value);
+        return GEMM_OK;
+    case GEMM_OPT_TC_STAGE_SLICES:
+        if (value < 0 || value > 2) break;
+        h->tc_slices = static_cast<int>(value);
         return GEMM_OK;
     case GEMM_OPT_SPLIT_K:
         if (value < 0 || value > 64) break;

@@ -110,9 +110,12 @@ size_t tc_partial_bytes(int64_t M, int64_t N, const TcSplit &sp);
 // {128-byte column chunk, K, chunk index} with a box of the columns one CTA
 // stages (kTcBN, or kTcBN/2 in a pair), fetched by one TMA instruction per
 // stage instead of one per chunk.
+// wide (pair MMA mode without a K split): three ring stages of two 128-byte
+// K slices each instead of six of one (same tensor maps and boxes).
 cudaError_t launch_tc(int dtype, int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB,
                       const CUtensorMap *tmC, int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
-                      const LaunchCommon &lc, int cluster, bool b_chunks, const TcSplit &sp = TcSplit());
+                      const LaunchCommon &lc, int cluster, bool b_chunks, const TcSplit &sp = TcSplit(),
+                      bool wide = false);
 
 // Persistent grid of the tensor-core kernel: one CTA per SM, whole clusters.
 int tc_grid(int64_t M, int64_t N, int sm_count, int cluster, int splits = 1);

@@ -260,14 +260,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // Whole warp, warp-uniform stage indices and descriptors; one elected
+        // lane issues (as in the pair kernel below).
+        {
             uint32_t it = 0, acc_it = 0;
             bool ok = true, issued = false;
             for (int u = cluster; ok && u < num_units; u += clusters, ++acc_it) {
                 const uint32_t abuf = acc_it & 1u;
                 const uint32_t aph = (acc_it >> 1) & 1u;
-                if (!mbar_wait(tempty_bar + 8 * abuf, aph ^ 1u, abort_flag, p.status,
-                               kWaitMmaTmemEmpty, p.timeout_ns)) {
+                if (!mbar_wait_warp(tempty_bar + 8 * abuf, aph ^ 1u, abort_flag, p.status, kWaitMmaTmemEmpty,
+                                    p.timeout_ns)) {
                     ok = false;
                     break;
                 }
@@ -277,37 +279,42 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int kt = kr.kt0; kt < kr.kt1; ++kt, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
-                    if (!mbar_wait(full_bar + 8 * s, ph, abort_flag, p.status, kWaitMmaFull,
-                                   p.timeout_ns)) {
+                    if (!mbar_wait_warp(full_bar + 8 * s, ph, abort_flag, p.status, kWaitMmaFull, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
                     const uint32_t a_st = sbase + s * STAGE_BYTES;
                     const uint32_t b_st = a_st + A_BYTES;
+                    uint64_t ad[K_STEPS], bd[K_STEPS];
 #pragma unroll
                     for (int kk = 0; kk < K_STEPS; ++kk) {
-                        const uint64_t adesc = smem_desc(a_st + kk * 32, 16, 1024, kLayoutSw128);
-                        const uint64_t bdesc =
-                            LAYOUT_B == 0
-                                ? smem_desc(b_st + kk * UMMA_K * 128, BOX_BYTES, B_MN_SBO, B_MN_LAYOUT)
-                                : smem_desc(b_st + kk * 32, 16, 1024, kLayoutSw128);
-                        const uint32_t accumulate = (kt > kr.kt0 || kk > 0) ? 1u : 0u;
-                        if (DT == 0)
-                            tc_mma_f16(d_tmem, adesc, bdesc, IDESC, accumulate);
-                        else
-                            tc_mma_tf32(d_tmem, adesc, bdesc, IDESC, accumulate);
+                        ad[kk] = smem_desc(a_st + kk * 32, 16, 1024, kLayoutSw128);
+                        bd[kk] = LAYOUT_B == 0 ? smem_desc(b_st + kk * UMMA_K * 128, BOX_BYTES, B_MN_SBO, B_MN_LAYOUT)
+                                               : smem_desc(b_st + kk * 32, 16, 1024, kLayoutSw128);
                     }
+                    const uint32_t acc0 = kt > kr.kt0 ? 1u : 0u;
+                    if (elect_one()) {
+#pragma unroll
+                        for (int kk = 0; kk < K_STEPS; ++kk) {
+                            if (DT == 0)
+                                tc_mma_f16(d_tmem, ad[kk], bd[kk], IDESC, kk > 0 ? 1u : acc0);
+                            else
+                                tc_mma_tf32(d_tmem, ad[kk], bd[kk], IDESC, kk > 0 ? 1u : acc0);
+                        }
+                        if (CL == 1)
+                            tc_commit(empty_bar + 8 * s);
+                        else
+                            tc_commit_multicast(empty_bar + 8 * s, CLUSTER_MASK);
+                    }
+                    __syncwarp();
                     issued = true;
-                    if (CL == 1)
-                        tc_commit(empty_bar + 8 * s);
-                    else
-                        tc_commit_multicast(empty_bar + 8 * s, CLUSTER_MASK);
                 }
                 if (!ok) break;
-                tc_commit(tfull_bar + 8 * abuf);
+                if (elect_one()) tc_commit(tfull_bar + 8 * abuf);
+                __syncwarp();
             }
-            if (!ok && issued) {
+            if (!ok && issued && lane == 0) {
                 // Let every MMA already issued finish before TMEM is freed.
                 tc_commit(drain_bar);
                 int dummy = 0;
@@ -416,31 +423,48 @@ __global__ void __launch_bounds__(THREADS, 1)
 // ---------------------------------------------------------------------------
 // Pair kernel: one 256 x 256 tile per cluster of two CTAs, computed by
 // tcgen05.mma.cta_group::2 issued from the even CTA.  Each CTA stages only
-// its 128 rows of A and its 128 columns of B (32 KB per stage instead of
-// 48 KB), so six stages fit where the one-CTA kernel holds four: more bytes
-// in flight per unit of MMA work.  D rows of CTA r live in CTA r's TMEM.
-constexpr int P_STAGES = 6;
-constexpr int P_A_BYTES = BM * 128;        // 16 KiB
-constexpr int P_B_BYTES = (BN / 2) * 128;  // 16 KiB: this CTA's half of B
-constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
-constexpr int P_NUM_BARS = 2 * P_STAGES + 2 + 2 + 1;
-constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + EPI_BYTES + P_NUM_BARS * 8 + 16;
-static_assert(P_STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
-static_assert(P_SMEM_BYTES > 116 * 1024 && P_SMEM_BYTES <= 227 * 1024, "one CTA per SM");
+// its 128 rows of A and its 128 columns of B (32 KB per 128-byte slice of K
+// instead of 48 KB), so 192 KB of operands are in flight per SM.  D rows of
+// CTA r live in CTA r's TMEM.
+//
+// SUB = K slices of 128 bytes per ring stage.  SUB = 1: six stages of one
+// slice (4 MMA instructions between a full-barrier wait and a release).
+// SUB = 2: three stages of two slices (8 MMAs per wait and release), the
+// same bytes in flight with half the barrier round trips per MMA; the MMA
+// issuer is a single thread whose per-stage wait and commit cost shows up
+// directly as idle tensor-pipe cycles, so fewer, larger stages keep the
+// pipe busier.
+constexpr int P_A_BYTES = BM * 128;        // 16 KiB per slice
+constexpr int P_B_BYTES = (BN / 2) * 128;  // 16 KiB per slice: this CTA's half of B
+constexpr int P_RING_BYTES = 6 * (P_A_BYTES + P_B_BYTES);
 
-template <int DT, int LAYOUT_B>
+template <int SUB>
+struct PairCfg {
+    static constexpr int STAGE_BYTES = SUB * (P_A_BYTES + P_B_BYTES);
+    static constexpr int STAGES = P_RING_BYTES / STAGE_BYTES;
+    static constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8 + 16;
+    static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+    static_assert(SMEM_BYTES > 116 * 1024 && SMEM_BYTES <= 227 * 1024, "one CTA per SM");
+};
+
+template <int DT, int LAYOUT_B, int SUB>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const TcParams p)
 {
     constexpr int ES = DT == 0 ? 2 : 4;
-    constexpr int BK = 128 / ES;
+    constexpr int BK_SLICE = 128 / ES;           // K elements per 128-byte slice
+    constexpr int BK = SUB * BK_SLICE;           // K elements per stage
     constexpr int UMMA_K = 32 / ES;
-    constexpr int K_STEPS = BK / UMMA_K;
+    constexpr int K_STEPS = BK_SLICE / UMMA_K;   // MMA instructions per slice
+    constexpr int P_STAGES = PairCfg<SUB>::STAGES;
+    constexpr int P_STAGE_BYTES = PairCfg<SUB>::STAGE_BYTES;
+    constexpr int P_NUM_BARS = PairCfg<SUB>::NUM_BARS;
     constexpr int BOX_N = 128 / ES;              // row-major B: N elements per TMA box
     constexpr int B_HALF_BOXES = (BN / 2) / BOX_N;
-    constexpr int BOX_BYTES = BK * 128;
+    constexpr int BOX_BYTES = BK_SLICE * 128;
     // M = 256 across the pair, N = 256.
     constexpr uint32_t IDESC = (1u << 4) | ((DT == 0 ? 1u : 2u) << 7) | ((DT == 0 ? 1u : 2u) << 10) |
                                ((LAYOUT_B == 0 ? 1u : 0u) << 16) | (static_cast<uint32_t>(BN >> 3) << 17) |
@@ -518,24 +542,31 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t fb_local = full_bar + 8 * s;
                     const uint32_t fb = mapa_shared(fb_local, 0);  // the even CTA's barrier
                     const uint32_t a_st = sbase + s * P_STAGE_BYTES;
-                    const uint32_t b_st = a_st + P_A_BYTES;
+                    const uint32_t b_st = a_st + SUB * P_A_BYTES;
                     if (leader) mbar_arrive_expect_tx(fb_local, 2 * P_STAGE_BYTES);
                     if (p.debug_drop && blockIdx.x == 0 && it == 0) continue;  // bytes that never come
-                    tma_load_2d_pair(a_st, &tmA, fb, kt * BK, mb * BM);
                     const int n_half = nb * BN + static_cast<int>(rank) * (BN / 2);
-                    if (LAYOUT_B == 0) {
-                        if (p.b_chunks) {
-                            // {column in chunk, k, chunk}: the B_HALF_BOXES chunks of
-                            // this CTA's half land one after another, as the 2-D
-                            // boxes would (the swizzle follows the address)
-                            tma_load_3d_pair(b_st, &tmB, fb, 0, kt * BK, n_half / BOX_N);
-                        } else {
 #pragma unroll
-                            for (int j = 0; j < B_HALF_BOXES; ++j)
-                                tma_load_2d_pair(b_st + j * BOX_BYTES, &tmB, fb, n_half + j * BOX_N, kt * BK);
+                    for (int sl = 0; sl < SUB; ++sl) {
+                        // slice sl of the stage: K elements [kx, kx + BK_SLICE)
+                        const int kx = kt * BK + sl * BK_SLICE;
+                        const uint32_t a_sl = a_st + sl * P_A_BYTES;
+                        const uint32_t b_sl = b_st + sl * P_B_BYTES;
+                        tma_load_2d_pair(a_sl, &tmA, fb, kx, mb * BM);
+                        if (LAYOUT_B == 0) {
+                            if (p.b_chunks) {
+                                // {column in chunk, k, chunk}: the B_HALF_BOXES chunks of
+                                // this CTA's half land one after another, as the 2-D
+                                // boxes would (the swizzle follows the address)
+                                tma_load_3d_pair(b_sl, &tmB, fb, 0, kx, n_half / BOX_N);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < B_HALF_BOXES; ++j)
+                                    tma_load_2d_pair(b_sl + j * BOX_BYTES, &tmB, fb, n_half + j * BOX_N, kx);
+                            }
+                        } else {
+                            tma_load_2d_pair(b_sl, &tmB, fb, kx, n_half);
                         }
-                    } else {
-                        tma_load_2d_pair(b_st, &tmB, fb, kt * BK, n_half);
                     }
                 }
             }
@@ -559,14 +590,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer (even CTA)
-        if (leader && lane == 0) {
+        // The whole warp runs the loop, so stage indices and descriptors are
+        // warp-uniform values; one elected lane issues a stage's MMAs and its
+        // commit.  The issue rate of this one warp bounds the tensor pipe
+        // (four MMAs of 128 cycles per stage), and the warp-uniform form
+        // issues them in about half the time of a single-lane loop.
+        if (leader) {
             uint32_t it = 0, acc_it = 0;
             bool ok = true, issued = false;
             for (int u = cluster; ok && u < num_units; u += clusters, ++acc_it) {
                 const uint32_t abuf = acc_it & 1u;
                 const uint32_t aph = (acc_it >> 1) & 1u;
-                if (!mbar_wait(tempty_bar + 8 * abuf, aph ^ 1u, abort_flag, p.status,
-                               kWaitMmaTmemEmpty, p.timeout_ns)) {
+                if (!mbar_wait_warp(tempty_bar + 8 * abuf, aph ^ 1u, abort_flag, p.status, kWaitMmaTmemEmpty,
+                                    p.timeout_ns)) {
                     ok = false;
                     break;
                 }
@@ -576,34 +612,41 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int kt = kr.kt0; kt < kr.kt1; ++kt, ++it) {
                     const uint32_t s = it % P_STAGES;
                     const uint32_t ph = (it / P_STAGES) & 1u;
-                    if (!mbar_wait(full_bar + 8 * s, ph, abort_flag, p.status, kWaitMmaFull,
-                                   p.timeout_ns)) {
+                    if (!mbar_wait_warp(full_bar + 8 * s, ph, abort_flag, p.status, kWaitMmaFull, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
                     const uint32_t a_st = sbase + s * P_STAGE_BYTES;
-                    const uint32_t b_st = a_st + P_A_BYTES;
+                    const uint32_t b_st = a_st + SUB * P_A_BYTES;
+                    uint64_t ad[SUB * K_STEPS], bd[SUB * K_STEPS];
 #pragma unroll
-                    for (int kk = 0; kk < K_STEPS; ++kk) {
-                        const uint64_t adesc = smem_desc(a_st + kk * 32, 16, 1024, kLayoutSw128);
-                        const uint64_t bdesc =
-                            LAYOUT_B == 0
-                                ? smem_desc(b_st + kk * UMMA_K * 128, BOX_BYTES, B_MN_SBO, B_MN_LAYOUT)
-                                : smem_desc(b_st + kk * 32, 16, 1024, kLayoutSw128);
-                        const uint32_t accumulate = (kt > kr.kt0 || kk > 0) ? 1u : 0u;
-                        if (DT == 0)
-                            tc_mma_f16_pair(d_tmem, adesc, bdesc, IDESC, accumulate);
-                        else
-                            tc_mma_tf32_pair(d_tmem, adesc, bdesc, IDESC, accumulate);
+                    for (int q = 0; q < SUB * K_STEPS; ++q) {
+                        const int sl = q / K_STEPS, kk = q % K_STEPS;
+                        ad[q] = smem_desc(a_st + sl * P_A_BYTES + kk * 32, 16, 1024, kLayoutSw128);
+                        bd[q] = LAYOUT_B == 0 ? smem_desc(b_st + sl * P_B_BYTES + kk * UMMA_K * 128, BOX_BYTES,
+                                                          B_MN_SBO, B_MN_LAYOUT)
+                                              : smem_desc(b_st + sl * P_B_BYTES + kk * 32, 16, 1024, kLayoutSw128);
                     }
+                    const uint32_t acc0 = kt > kr.kt0 ? 1u : 0u;
+                    if (elect_one()) {
+#pragma unroll
+                        for (int q = 0; q < SUB * K_STEPS; ++q) {
+                            if (DT == 0)
+                                tc_mma_f16_pair(d_tmem, ad[q], bd[q], IDESC, q > 0 ? 1u : acc0);
+                            else
+                                tc_mma_tf32_pair(d_tmem, ad[q], bd[q], IDESC, q > 0 ? 1u : acc0);
+                        }
+                        tc_commit_pair_multicast(empty_bar + 8 * s, 0x3);
+                    }
+                    __syncwarp();
                     issued = true;
-                    tc_commit_pair_multicast(empty_bar + 8 * s, 0x3);
                 }
                 if (!ok) break;
-                tc_commit_pair_multicast(tfull_bar + 8 * abuf, 0x3);
+                if (elect_one()) tc_commit_pair_multicast(tfull_bar + 8 * abuf, 0x3);
+                __syncwarp();
             }
-            if (!ok && issued) {
+            if (!ok && issued && lane == 0) {
                 tc_commit_pair_multicast(drain_bar, 0x1);
                 int dummy = 0;
                 mbar_wait(drain_bar, 0, &dummy, nullptr, kWaitDrain, p.timeout_ns);
@@ -706,21 +749,21 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
-template <int DT, int L>
+template <int DT, int L, int SUB>
 cudaError_t set_pair_attrs()
 {
-    return cudaFuncSetAttribute(gemm_tc_pair_kernel<DT, L>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                P_SMEM_BYTES);
+    return cudaFuncSetAttribute(gemm_tc_pair_kernel<DT, L, SUB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                PairCfg<SUB>::SMEM_BYTES);
 }
 
-template <int DT, int L>
+template <int DT, int L, int SUB>
 cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                         const TcParams &p, int grid, cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = P_SMEM_BYTES;
+    cfg.dynamicSmemBytes = PairCfg<SUB>::SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -729,7 +772,7 @@ cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<DT, L>, tmA, tmB, tmC, p);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<DT, L, SUB>, tmA, tmB, tmC, p);
 }
 
 template <int DT, int L, int CL>
@@ -769,8 +812,9 @@ cudaError_t prepare_tc()
     cudaError_t e = cudaSuccess;
     cudaError_t (*fns[])() = {set_attrs<0, 0, 1>, set_attrs<0, 1, 1>, set_attrs<1, 0, 1>, set_attrs<1, 1, 1>,
                               set_attrs<0, 0, 2>, set_attrs<0, 1, 2>, set_attrs<1, 0, 2>, set_attrs<1, 1, 2>,
-                              set_pair_attrs<0, 0>, set_pair_attrs<0, 1>, set_pair_attrs<1, 0>,
-                              set_pair_attrs<1, 1>};
+                              set_pair_attrs<0, 0, 1>, set_pair_attrs<0, 1, 1>, set_pair_attrs<1, 0, 1>,
+                              set_pair_attrs<1, 1, 1>, set_pair_attrs<0, 0, 2>, set_pair_attrs<0, 1, 2>,
+                              set_pair_attrs<1, 0, 2>, set_pair_attrs<1, 1, 2>};
     for (auto f : fns)
         if (e == cudaSuccess) e = f();
     return e;
@@ -826,7 +870,7 @@ size_t tc_partial_bytes(int64_t M, int64_t N, const TcSplit &sp)
 
 cudaError_t launch_tc(int dtype, int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB,
                       const CUtensorMap *tmC, int M, int N, int K, float *C, int64_t ldc, bool c_vec4,
-                      const LaunchCommon &lc, int cluster, bool b_chunks, const TcSplit &sp)
+                      const LaunchCommon &lc, int cluster, bool b_chunks, const TcSplit &sp, bool wide)
 {
     TcParams p;
     p.M = M;
@@ -846,17 +890,24 @@ cudaError_t launch_tc(int dtype, int layout_b, const CUtensorMap &tmA, const CUt
     p.b_chunks = b_chunks && (cluster == 3 || cluster == 1) && layout_b == 0 ? 1 : 0;
     p.debug_drop = lc.debug_drop;
     const bool split = sp.splits > 1 && cluster != 2;
+    wide = wide && !split;
     p.splits = split ? sp.splits : 1;
     p.kt_per_split = split ? sp.kt_per_split : (K + (128 / (dtype == GEMM_BF16 ? 2 : 4)) - 1) / (128 / (dtype == GEMM_BF16 ? 2 : 4));
     if (p.kt_per_split < 1) p.kt_per_split = 1;
     p.partials = split ? sp.partials : nullptr;
     const CUtensorMap &tc = tmC != nullptr ? *tmC : tmA;  // unused when c_tma == 0
     const bool bf16 = dtype == GEMM_BF16;
+    if (cl == 3 && wide) {
+        if (bf16) return layout_b == 0 ? launch_pair<0, 0, 2>(tmA, tmB, tc, p, lc.grid, lc.stream)
+                                       : launch_pair<0, 1, 2>(tmA, tmB, tc, p, lc.grid, lc.stream);
+        return layout_b == 0 ? launch_pair<1, 0, 2>(tmA, tmB, tc, p, lc.grid, lc.stream)
+                             : launch_pair<1, 1, 2>(tmA, tmB, tc, p, lc.grid, lc.stream);
+    }
     if (cl == 3) {
-        if (bf16) return layout_b == 0 ? launch_pair<0, 0>(tmA, tmB, tc, p, lc.grid, lc.stream)
-                                       : launch_pair<0, 1>(tmA, tmB, tc, p, lc.grid, lc.stream);
-        return layout_b == 0 ? launch_pair<1, 0>(tmA, tmB, tc, p, lc.grid, lc.stream)
-                             : launch_pair<1, 1>(tmA, tmB, tc, p, lc.grid, lc.stream);
+        if (bf16) return layout_b == 0 ? launch_pair<0, 0, 1>(tmA, tmB, tc, p, lc.grid, lc.stream)
+                                       : launch_pair<0, 1, 1>(tmA, tmB, tc, p, lc.grid, lc.stream);
+        return layout_b == 0 ? launch_pair<1, 0, 1>(tmA, tmB, tc, p, lc.grid, lc.stream)
+                             : launch_pair<1, 1, 1>(tmA, tmB, tc, p, lc.grid, lc.stream);
     }
     if (cl == 1) {
         if (bf16) return layout_b == 0 ? launch_one<0, 0, 1>(tmA, tmB, tc, p, lc.grid, lc.stream)

@@ -244,6 +244,28 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
                  : "memory");
 }
 
+// One lane of the (fully active) warp gets true.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
+// mbar_wait for a whole warp: every lane gets the same result.  The fast
+// path is one try_wait per lane and a vote; otherwise lane 0 waits (bounded)
+// and broadcasts the outcome, so the warp never diverges on a timeout.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int *abort, int *status,
+                                               int site, uint64_t timeout_ns)
+{
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, status, site, timeout_ns) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {
     uint32_t r;

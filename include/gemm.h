@@ -113,6 +113,11 @@ extern "C" {
  * host buffers) fails with GEMM_ERR_NOMEM before launching anything; an
  * allocation already made is kept. */
 #define GEMM_OPT_WORKSPACE_LIMIT 12
+/* Pair-MMA tensor-core mode without a K split: 128-byte K slices per stage
+ * of its shared-memory ring.  1 = six stages of one slice; 2 = three stages
+ * of two slices (the same bytes in flight, half the barrier round trips per
+ * MMA instruction); 0 (default) = chosen by the library.  Same results. */
+#define GEMM_OPT_TC_STAGE_SLICES 13
 
 typedef struct gemm_ctx *gemm_handle_t;
 

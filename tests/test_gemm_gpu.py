@@ -441,6 +441,33 @@ def test_cluster_pairs_match_oracle_and_single_cta(g, oracle_mod, cluster_mode, 
     assert torch.equal(C1, C2)
 
 
+@pytest.mark.parametrize("mode", ["tf32", "bf16"])
+@pytest.mark.parametrize("layout", [ROW, COL])
+@pytest.mark.parametrize("shape", CLUSTER_SHAPES + [(520, 300, 33), (600, 512, 200), (300, 256, 1000)])
+def test_pair_wide_stages_same_bits(g, oracle_mod, mode, layout, shape):
+    """Pair MMA with two 128-byte K slices per ring stage (three stages)
+    against one slice per stage (six stages): the MMA instructions run in the
+    same K order, so the bits are the same; K lengths that end inside a
+    stage, or inside its first slice, take zero-filled slices."""
+    from dense_gemm_sm100_gb300 import gemm
+    M, N, K = shape
+    A, B = inp.make_operands(M, N, K, layout_b=layout, dist="normal", seed=2 * M + N + 5 * K, dtype=mode)
+    g.set_option(gemm.GEMM_OPT_SPLIT_K, 1)
+    try:
+        g.set_option(gemm.GEMM_OPT_TC_STAGE_SLICES, 1)
+        C1 = run_gpu(g, A, B, layout, mode).cpu()
+        assert "pair256x256_" in g.last_path, g.last_path
+        g.set_option(gemm.GEMM_OPT_TC_STAGE_SLICES, 2)
+        C2 = run_gpu(g, A, B, layout, mode).cpu()
+        assert "pair256x256w_" in g.last_path, g.last_path
+    finally:
+        g.set_option(gemm.GEMM_OPT_TC_STAGE_SLICES, 0)
+        g.set_option(gemm.GEMM_OPT_SPLIT_K, 0)
+    Cr, S = oracle_of(oracle_mod, A, B, layout)
+    assert_parity(C2, Cr, S, TOL[mode], f"wide stages {mode} {shape}")
+    assert torch.equal(C1, C2)
+
+
 # ------------------------------------------------------- split-K (FP32 path)
 
 SIMT_CONFIG_SHAPES = [(1, 1, 1), (129, 257, 33), (300, 520, 260), (640, 1030, 512)]
