@@ -265,14 +265,12 @@ def bench_workload(g, name, steps, warmup, dist_ctx, peaks, peak_note, with_e2e,
         # same stream and power state.  Never part of this library's path.
         torch.backends.cuda.matmul.allow_tf32 = w.dtype == "tf32"
         Bl = B_d if w.layout_b == 0 else B_d.t()
-        Af = A_d if w.dtype != "bf16" else A_d
-        cub_ms, _, _ = time_device(lambda: torch.matmul(Af, Bl), stream, max(5, steps // 2), warmup)
+        fn, what = cublas_side_call(A_d, Bl, w.dtype)
+        cub_ms, _, _ = time_device(fn, stream, max(5, steps // 2), warmup)
         torch.backends.cuda.matmul.allow_tf32 = False
         res["cublas_side"] = {
             "tflops": w.flops / (cub_ms / max(5, steps // 2) * 1e-3) / 1e12,
-            "what": "torch.matmul (cuBLAS) on the same operands; " +
-                    ("BF16 output (cuBLAS default), not FP32" if w.dtype == "bf16" else
-                     "TF32 math allowed" if w.dtype == "tf32" else "FP32, TF32 disallowed"),
+            "what": "cuBLAS through torch on the same operands; " + what,
         }
     if with_e2e:
         Ah = A.pin_memory()
@@ -294,6 +292,21 @@ def bench_workload(g, name, steps, warmup, dist_ctx, peaks, peak_note, with_e2e,
     del A_d, B_d, C_d
     torch.cuda.empty_cache()
     return res
+
+
+def cublas_side_call(A_d, B_view, dtype):
+    """The labelled cuBLAS side reference for one workload: a callable and
+    what it computes.  BF16 inputs ask for FP32 output (torch.mm out_dtype),
+    as this library writes; without that overload, BF16 output, said so."""
+    import torch
+    if dtype == "bf16":
+        try:
+            torch.mm(A_d[:8, :8], B_view[:8, :8], out_dtype=torch.float32)
+            return (lambda: torch.mm(A_d, B_view, out_dtype=torch.float32)), "BF16 inputs, FP32 output"
+        except (TypeError, RuntimeError):
+            return (lambda: torch.matmul(A_d, B_view)), "BF16 inputs, BF16 output (no FP32-output overload)"
+    what = "TF32 math allowed, FP32 output" if dtype == "tf32" else "FP32, TF32 disallowed"
+    return (lambda: torch.matmul(A_d, B_view)), what
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -494,7 +507,8 @@ def run_configs(args):
         # labelled side reference: cuBLAS through torch on the same operands
         torch.backends.cuda.matmul.allow_tf32 = w.dtype == "tf32"
         Bl = B_d if w.layout_b == 0 else B_d.t()
-        _, cub, _ = time_device(lambda: torch.matmul(A_d, Bl), stream, steps, args.warmup)
+        cub_fn, cub_what = cublas_side_call(A_d, Bl, w.dtype)
+        _, cub, _ = time_device(cub_fn, stream, steps, args.warmup)
         torch.backends.cuda.matmul.allow_tf32 = False
         tf = lambda ms: round(w.flops / (ms * 1e-3) / 1e12, 3)
         out.append({"workload": name, "description": DESCRIPTIONS.get(name, name), "dtype": w.dtype,
@@ -505,9 +519,7 @@ def run_configs(args):
                                     "tflops_median": tf(statistics.median(cold)),
                                     "tflops_max": tf(min(cold))},
                     "cublas_side": {"tflops_median": tf(statistics.median(cub)),
-                                    "what": "torch.matmul (cuBLAS), warm, " +
-                                            ("BF16 output" if w.dtype == "bf16" else
-                                             "TF32 allowed" if w.dtype == "tf32" else "TF32 off")}})
+                                    "what": "cuBLAS through torch, warm, " + cub_what}})
         if args.results:
             with open(args.results, "a") as f:
                 f.write(json.dumps(out[-1]) + "\n")

@@ -879,8 +879,18 @@ cudaError_t launch_tc(int dtype, int layout_b, const CUtensorMap &tmA, const CUt
     p.tiles_m = (M + BM - 1) / BM;
     p.tiles_n = (N + BN - 1) / BN;
     const int cl = cluster == 2 ? 2 : cluster == 3 ? 3 : 1;
-    // group_m counts units (tile rows, or tile-row pairs for clusters) along M
-    p.group_m = lc.group_m > 0 ? lc.group_m : (cl >= 2 ? 8 : 16);
+    // group_m counts units (tile rows, or tile-row pairs for clusters) along M.
+    // Pair MMA: the largest group whose A panel (group x 256 rows x K) stays
+    // within 32 MB, a quarter of L2, so it is read from DRAM once while the
+    // group sweeps the columns of B ("GEMM 性能优化", Wave 模型与 L2 命中率);
+    // 16 for BF16 and 8 for TF32 at K = 4096 (measured best, FFN shape).
+    int dflt = cl >= 2 ? 8 : 16;
+    if (cl == 3) {
+        const int64_t panel = int64_t{2 * BM} * K * (dtype == GEMM_BF16 ? 2 : 4);
+        const int64_t fit = panel > 0 ? (int64_t{32} << 20) / panel : 16;
+        dflt = static_cast<int>(fit < 4 ? 4 : fit > 16 ? 16 : fit);
+    }
+    p.group_m = lc.group_m > 0 ? lc.group_m : dflt;
     p.C = C;
     p.ldc = ldc;
     p.status = lc.status;
