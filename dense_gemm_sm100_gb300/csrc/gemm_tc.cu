@@ -6,10 +6,11 @@
 // the Blackwell form of that step:
 //  * warp 0, one thread: TMA producer filling a 4-stage shared-memory ring
 //    (128-byte swizzled rows of A and B) guarded by full/empty mbarriers;
-//  * warp 1: allocates 512 TMEM columns (two 128x256 FP32 accumulators) and,
-//    from one thread, issues tcgen05.mma (M=128, N=256, K=32 bytes per
-//    instruction); tcgen05.commit releases ring stages and announces a
-//    finished accumulator;
+//  * warp 1: allocates 512 TMEM columns (two 128x256 FP32 accumulators) and
+//    runs the MMA loop as a whole warp (warp-uniform stage indices and
+//    descriptors); one elected lane issues tcgen05.mma (M=128, N=256, K=32
+//    bytes per instruction) and tcgen05.commit, which releases ring stages
+//    and announces a finished accumulator;
 //  * warps 2-5: epilogue, tcgen05.ld of their 32 TMEM lanes; each 32x32 FP32
 //    chunk is staged in 128-byte-swizzled shared memory and written by one
 //    TMA store (whole 128-byte lines; TMA clips the M and N edges).  With two
