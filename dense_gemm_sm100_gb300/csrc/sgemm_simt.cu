@@ -705,13 +705,16 @@ void launch_cfg(int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB, co
 // TFLOP/s measured on GB300 at sizes that fill whole waves (M = 7296 or
 // 14592, N = 8192); simt_pick_config weighs them against each shape's
 // waves.  The scalar-FMA, 64x128 and 64x64 tiles (56.4, 59.2 and 31.5 at
-// 8192^3), 128x256 with register reallocation (8x16 per thread, 64.0), 16
-// consumer warps of 8x4 (64.4) and 16 consumer warps of 8x8 with A loaded
-// in pairs (256x128, 112 registers, spills: 59.3) never win; they stay
-// selectable.  12 consumer warps (3 per scheduler, 192x128) hide the
-// multiply-add latency better than 8 (67.4 against 64.4; column-major B,
-// its corner turn shared by the four producer warps, 62.3 against 60.0);
-// with scalar FMAs instead of packed pairs the same tile is issue-bound
+// 8192^3), 128x256 with register reallocation (8x16 per thread, 64.0) and
+// 16 consumer warps of 8x8 with A loaded in pairs (256x128, 112 registers,
+// spills: 59.3) never win; they stay selectable.  More consumer warps per
+// scheduler hide the multiply-add latency better: 12 (3 per scheduler,
+// 192x128) against 8, 67.4 against 64.4 (column-major B, its corner turn
+// shared by the four producer warps, 62.3 against 60.0), and for 128x128
+// tiles 16 warps of 8x4 (4 per scheduler, register reallocation) against 8
+// of 8x8, 66.4 against 64.4 with row-major B (2-3 % on every shape
+// measured, 4095x3073x2047 included) but 59.2 against 60.0 column-major.
+// With scalar FMAs instead of packed pairs the 192x128 tile is issue-bound
 // (57.7).
 ConfigEntry g_configs[] = {
     DG_SIMT_CFG(4, 2, 8, 6, 8, 1, 0, 64.9f, 60.0f, "128x128"),
@@ -720,7 +723,7 @@ ConfigEntry g_configs[] = {
     DG_SIMT_CFG(2, 1, 8, 4, 8, 1, 0, 0.0f, 0.0f, "64x64"),
     DG_SIMT_CFG(4, 2, 16, 4, 8, 1, 1, 0.0f, 0.0f, "128x256r"),
     DG_SIMT_CFG(6, 2, 8, 4, 8, 1, 1, 67.3f, 62.3f, "192x128r"),
-    DG_SIMT_CFG(4, 4, 4, 6, 8, 1, 1, 0.0f, 0.0f, "128x128w16"),
+    DG_SIMT_CFG(4, 4, 4, 6, 8, 1, 1, 66.4f, 0.0f, "128x128w16"),
     DG_SIMT_CFG(8, 2, 8, 4, 8, 1, 1, 0.0f, 0.0f, "256x128r"),
 };
 constexpr int kNumConfigs = sizeof(g_configs) / sizeof(g_configs[0]);

@@ -116,7 +116,8 @@ extern "C" {
 /* Pair-MMA tensor-core mode without a K split: 128-byte K slices per stage
  * of its shared-memory ring.  1 = six stages of one slice; 2 = three stages
  * of two slices (the same bytes in flight, half the barrier round trips per
- * MMA instruction); 0 (default) = chosen by the library.  Same results. */
+ * MMA instruction); 0 (default) = the library's choice, at present six
+ * stages of one slice (faster on every shape measured).  Same results. */
 #define GEMM_OPT_TC_STAGE_SLICES 13
 
 typedef struct gemm_ctx *gemm_handle_t;
