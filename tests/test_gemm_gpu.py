@@ -497,6 +497,29 @@ def test_simt_configs_match_oracle(g, oracle_mod, config, layout, shape):
 
 
 @pytest.mark.parametrize("layout", [ROW, COL])
+@pytest.mark.parametrize("shape", [(129, 257, 300), (640, 1030, 512), (385, 200, 1001)])
+def test_simt_configs_same_bits(g, layout, shape):
+    """Without a K split every FP32 configuration adds each element's
+    products in k order with one FMA per product (8x8 or 8x4 thread tiles,
+    8, 12 or 16 consumer warps alike), so the dispatcher's choices give the
+    same bits: 128x128 with 8 warps (1), 192x128 (6), 128x128 with 16 warps
+    (7, the row-major 128x128 choice)."""
+    from dense_gemm_sm100_gb300 import gemm
+    M, N, K = shape
+    A, B = inp.make_operands(M, N, K, layout_b=layout, dist="normal", seed=M + N + K)
+    outs = []
+    g.set_option(gemm.GEMM_OPT_SPLIT_K, 1)
+    try:
+        for config in (1, 6, 7):
+            g.set_option(gemm.GEMM_OPT_SIMT_CONFIG, config)
+            outs.append(run_gpu(g, A, B, layout, "f32").cpu())
+    finally:
+        g.set_option(gemm.GEMM_OPT_SIMT_CONFIG, 0)
+        g.set_option(gemm.GEMM_OPT_SPLIT_K, 0)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+@pytest.mark.parametrize("layout", [ROW, COL])
 @pytest.mark.parametrize("splits", [2, 3, 7])
 def test_split_k_forced(g, oracle_mod, layout, splits):
     """K cut into slices whose partial products are summed in a second

@@ -1,7 +1,8 @@
 """Seeded random shapes across every path the dispatcher can take: all three
-modes, both B layouts, the FP32 tile configurations, the tensor-core CTA
-modes, and CTA caps that make the tail split and the tensor-core K split
-run on small problems, on device or host buffers.  Each result is checked
+modes, both B layouts, the FP32 tile configurations (128x128 with 8 or 16
+consumer warps, 192x128), the tensor-core CTA modes, and CTA caps that make
+the tail split and the tensor-core K split run on small problems, on device
+or host buffers.  Each result is checked
 against the oracle within the mode's tolerance; integer inputs must match
 exactly."""
 import random
@@ -27,7 +28,7 @@ def cases():
         M = rng.choice([1, 7, 64, 127, 128, 129, 200, 255, 256, 257, 383, 512, 700])
         N = rng.choice([1, 3, 32, 64, 100, 128, 129, 256, 257, 448, 520, 640])
         K = rng.choice([1, 5, 16, 31, 32, 33, 64, 100, 256, 333, 512, 1000])
-        simt_config = rng.choice([0, 0, 1, 6]) if mode == "f32" else 0
+        simt_config = rng.choice([0, 0, 1, 6, 7]) if mode == "f32" else 0
         tc_mode = rng.choice([1, 2, 3, 3]) if mode != "f32" else 3
         max_ctas = rng.choice([0, 0, 4, 8, 16])
         integer = rng.random() < 0.3
