@@ -46,9 +46,9 @@ NOMINAL_PF = {"bf16": 2.25, "tf32": 1.1}
 # ncu capture of the kernel as it is now; None until captured for this version.
 # Key: workload name -> (bytes per launch, summary file under profiles/).
 NCU_TRAFFIC: dict[str, tuple[float, str]] = {
-    "fp32_8192_row": (2716.0e6 + 260.8e6, "profiles/dram_traffic_full_size.md"),
-    "ffn_bf16_8192x14336x4096": (480.3e6 + 436.2e6, "profiles/dram_traffic_full_size.md"),
-    "ffn_tf32_8192x14336x4096": (2743.6e6 + 453.4e6, "profiles/dram_traffic_full_size.md"),
+    "fp32_8192_row": (2714.7e6 + 260.4e6, "profiles/dram_traffic_full_size.md"),
+    "ffn_bf16_8192x14336x4096": (481.4e6 + 434.8e6, "profiles/dram_traffic_full_size.md"),
+    "ffn_tf32_8192x14336x4096": (2202.0e6 + 454.1e6, "profiles/dram_traffic_full_size.md"),
 }
 
 DESCRIPTIONS = {
