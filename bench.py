@@ -33,14 +33,14 @@ if ROOT not in sys.path:
 METRIC = "GEMM TFLOPS (2MNK/t) and % of GB300 FP32-SIMT / tensor-core roofline"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "fp32_8192_row"
-TC_WORKLOADS = ["ffn_bf16_8192x14336x4096", "ffn_tf32_8192x14336x4096"]
+TC_WORKLOADS = ["ffn_bf16_8192x14336x4096", "ffn_tf32_8192x14336x4096", "fp32x3_8192_row"]
 
 # Fallback peaks (one earlier GB300 measurement) if MEASURED_PEAKS.json is absent.
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
             "sm_max_mhz": 2070.0}
 # Nominal dense tensor rates (PFLOP/s) used only to scale the measured BF16 peak
 # to TF32: a contraction is compared with the peak of its own input type.
-NOMINAL_PF = {"bf16": 2.25, "tf32": 1.1}
+NOMINAL_PF = {"bf16": 2.25, "tf32": 1.1, "f32x3": 1.1 / 3}  # f32x3: three TF32 products per FP32 one
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture of the kernel as it is now; None until captured for this version.
@@ -55,6 +55,8 @@ DESCRIPTIONS = {
     "fp32_8192_row": "FP32 SIMT GEMM M=N=K=8192, A/B/C row-major, U[-1,1) seed 3",
     "ffn_bf16_8192x14336x4096": "tensor-core GEMM, BF16 A/B, FP32 C, M=8192 N=14336 K=4096, N(0,0.02) seed 4",
     "ffn_tf32_8192x14336x4096": "tensor-core GEMM, TF32 (FP32 storage), FP32 C, M=8192 N=14336 K=4096, N(0,0.02) seed 4",
+    "fp32x3_8192_row": "FP32-accurate tensor-core GEMM (three TF32 products of split operands), M=N=K=8192, "
+                       "A/B/C row-major, U[-1,1) seed 3 (the FP32 workload's operands)",
     "fp32_1024_colB": "FP32 SIMT GEMM M=N=K=1024, B column-major, U[-1,1) seed 1",
     "fp32_4095x3073x2047_row": "FP32 SIMT GEMM M=4095 N=3073 K=2047, row-major, N(0,1) seed 2",
     "fp32_128_row": "FP32 SIMT GEMM M=N=K=128, row-major, U[-1,1) seed 0",
@@ -249,7 +251,9 @@ def bench_workload(g, name, steps, warmup, dist_ctx, peaks, peak_note, with_e2e,
                               f"derived: {sms} SMs x 128 FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz")
     else:
         peak = tensor_peak(w.dtype, peaks)
-        note = f"{peak_note} cuBLAS BF16 burst" + ("" if w.dtype == "bf16" else " x 1.1/2.25 (nominal TF32/BF16)")
+        note = f"{peak_note} cuBLAS BF16 burst" + {
+            "bf16": "", "tf32": " x 1.1/2.25 (nominal TF32/BF16)",
+            "f32x3": " x 1.1/2.25 / 3 (nominal TF32/BF16, three TF32 products per FP32 product)"}[w.dtype]
         roof = roofline_entry("tensor", achieved, peak, UNIT, NCU_TRAFFIC.get(name, (None,))[0], note)
     res = {
         "workload": name, "description": DESCRIPTIONS.get(name, name),
@@ -718,7 +722,10 @@ def main(argv=None):
             m = {k: r[k] for k in ("workload", "description", "dtype", "value",
                                    "ms_per_step", "kernel_ms", "path", "roofline")}
             if measured:
-                add_microbench(m["roofline"], measured.get(f"mma_{r['dtype']}_tflops"))
+                mb = measured.get(f"mma_{r['dtype']}_tflops")
+                if r["dtype"] == "f32x3" and measured.get("mma_tf32_tflops"):
+                    mb = measured["mma_tf32_tflops"] / 3
+                add_microbench(m["roofline"], mb)
             if "cublas_side" in r:
                 m["cublas_side"] = r["cublas_side"]
             if msampler:

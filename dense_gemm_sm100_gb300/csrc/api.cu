@@ -87,8 +87,8 @@ int check_args(int layout_b, int64_t M, int64_t N, int64_t K, const void *A, int
     };
     if (layout_b != GEMM_B_ROW_MAJOR && layout_b != GEMM_B_COL_MAJOR)
         return bad(GEMM_ERR_INVALID, "layout_b must be GEMM_B_ROW_MAJOR or GEMM_B_COL_MAJOR");
-    if (dtype != GEMM_F32 && dtype != GEMM_TF32 && dtype != GEMM_BF16)
-        return bad(GEMM_ERR_INVALID, "dtype must be GEMM_F32, GEMM_TF32 or GEMM_BF16");
+    if (dtype != GEMM_F32 && dtype != GEMM_TF32 && dtype != GEMM_BF16 && dtype != GEMM_F32_3XTF32)
+        return bad(GEMM_ERR_INVALID, "dtype must be GEMM_F32, GEMM_TF32, GEMM_BF16 or GEMM_F32_3XTF32");
     if (M < 0 || N < 0 || K < 0) return bad(GEMM_ERR_INVALID, "M, N and K must be >= 0");
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim)
         return bad(GEMM_ERR_INVALID, "M, N and K must be below 2^31 - 1024");
@@ -137,6 +137,27 @@ PackPlan plan_pack(const gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_
 {
     PackPlan pp;
     if (M == 0 || N == 0 || K == 0) return pp;
+    if (dtype == GEMM_F32_3XTF32) {
+        // The split operands always live in the workspace: A3 is M x 3K, B3
+        // 3K x N (row-major) or N x 3K (column-major), 16-byte pitches; then
+        // a TF32 product over 3K, planned as such.
+        const int64_t K3 = 3 * K;
+        const bool row = layout_b == GEMM_B_ROW_MAJOR;
+        pp.a = pp.b = true;
+        pp.lda = round_up(K3, 4);
+        pp.a_bytes = static_cast<size_t>(round_up(M * pp.lda * 4, 256));
+        pp.ldb = round_up(row ? N : K3, 4);
+        pp.b_bytes = static_cast<size_t>(round_up((row ? K3 : N) * pp.ldb * 4, 256));
+        const int cluster = tc_cluster_for(h, M);
+        if (cluster != 2) {
+            const int64_t ctas = h->max_ctas > 0 ? h->max_ctas : h->sm_count;
+            const int64_t slots = cluster == 3 ? ctas / 2 : ctas;
+            pp.tc_split = dg::tc_pick_splits(dg::tc_units(M, N, cluster), slots, K3, 4, h->split_k);
+            pp.split_bytes = static_cast<size_t>(
+                round_up(static_cast<int64_t>(dg::tc_partial_bytes(M, N, pp.tc_split)), 256));
+        }
+        return pp;
+    }
     const int es = elem_bytes(dtype);
     const int64_t align_elems = 16 / es;
     pp.a = h->force_repack || !tma_ready(A, lda, es);
@@ -295,7 +316,28 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
     uint8_t *ws = static_cast<uint8_t *>(h->ws) + ws_offset;
     const int64_t rows_b = layout_b == GEMM_B_ROW_MAJOR ? K : N;
     const int64_t cols_b = layout_b == GEMM_B_ROW_MAJOR ? N : K;
-    if (pp.a) {
+    const bool split3 = dtype == GEMM_F32_3XTF32;
+    if (split3) {
+        // FP32-accurate tensor-core mode: split A and B into TF32 parts
+        // (three along K) and run the TF32 path over 3K on them.
+        float *A3 = reinterpret_cast<float *>(ws);
+        float *B3 = reinterpret_cast<float *>(ws + pp.a_bytes);
+        cudaError_t e = dg::launch_split3(static_cast<const float *>(A), lda, A3, pp.lda, M, K, false, false,
+                                          h->sm_count, stream);
+        if (e == cudaSuccess)
+            e = dg::launch_split3(static_cast<const float *>(B), ldb, B3, pp.ldb, rows_b, cols_b,
+                                  layout_b == GEMM_B_ROW_MAJOR, true, h->sm_count, stream);
+        if (e != cudaSuccess) return cuda_fail(h, e, "operand split launch");
+        h->launches += 2;
+        A = A3;
+        lda = pp.lda;
+        B = B3;
+        ldb = pp.ldb;
+        K *= 3;
+        dtype = GEMM_TF32;
+        path += "+split3";
+    }
+    if (pp.a && !split3) {
         cudaError_t e = dg::launch_repack(A, lda, ws, pp.lda, M, K, es, h->sm_count, stream);
         if (e != cudaSuccess) return cuda_fail(h, e, "repack A launch");
         ++h->launches;
@@ -303,7 +345,7 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
         lda = pp.lda;
         path += "+repackA";
     }
-    if (pp.b) {
+    if (pp.b && !split3) {
         void *dst = ws + pp.a_bytes;
         cudaError_t e = dg::launch_repack(B, ldb, dst, pp.ldb, rows_b, cols_b, es, h->sm_count, stream);
         if (e != cudaSuccess) return cuda_fail(h, e, "repack B launch");
@@ -391,7 +433,7 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
                                       static_cast<int>(N), static_cast<int>(K), C, ldc, c_vec4, lc, cluster,
                                       b_chunks, sp, wide);
         if (e != cudaSuccess) return cuda_fail(h, e, "tensor-core kernel launch");
-        path = std::string(dtype == GEMM_BF16 ? "tc_bf16" : "tc_tf32") +
+        path = std::string(split3 ? "f32x3_tc_tf32" : dtype == GEMM_BF16 ? "tc_bf16" : "tc_tf32") +
                (cluster == 3 ? (wide ? "_pair256x256w_" : "_pair256x256_") : "_128x256_") + lay +
                (cluster == 2 ? "_cluster2" : "") +
                (b_chunks ? "+b3d" : "") + path;
@@ -598,7 +640,10 @@ HostBlocks plan_host_blocks(const gemm_ctx *h, int layout_b, int64_t M, int64_t 
     };
     // Rough rates of these kernels on all SMs and of the host link; they only
     // rank plans.  A wave takes as long with fewer slots (GEMM_OPT_MAX_CTAS).
-    const double rate = dtype == GEMM_F32 ? 64e12 : dtype == GEMM_TF32 ? 800e12 : 1650e12;  // FLOP/s
+    const double rate = dtype == GEMM_F32           ? 64e12
+                        : dtype == GEMM_TF32        ? 800e12
+                        : dtype == GEMM_F32_3XTF32 ? 270e12
+                                                    : 1650e12;  // FLOP/s
     const double link = 200e9;                                                             // bytes/s each way
     const double wave_s = 2.0 * bm * bn * K * full_slots / rate;
     const double h2d_all = (double(M) * K + double(K) * N) * es, d2h_all = double(M) * N * 4;

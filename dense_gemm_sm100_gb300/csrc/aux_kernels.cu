@@ -10,6 +10,12 @@
 //    kernels added in slice order ("GEMM 性能优化", 台阶 1: partial sums over K
 //    slices add up to the product).
 //  * zero fill: C = 0 for K = 0 (the empty sum).
+//  * three-part split of an FP32 operand for the FP32-accurate tensor-core
+//    mode: x = hi + lo with hi = x with its low 13 mantissa bits cleared (a
+//    TF32 value, exactly what the tensor core reads of hi) and lo = x - hi
+//    (exact in FP32).  The operand is written three times along K, so one
+//    TF32 product over 3K gives hi(A)hi(B) + hi(A)lo(B) + lo(A)hi(B), which
+//    is A·B up to the lo(A)lo(B) term (about 2^-22 of |a·b|).
 #include <cstdint>
 
 #include "gemm_internal.h"
@@ -26,6 +32,43 @@ __global__ void __launch_bounds__(256) repack_rows_kernel(const T *__restrict__ 
         const T *s = src + r * lds;
         T *d = dst + r * ldd;
         for (long long c = threadIdx.x; c < cols; c += blockDim.x) d[c] = s[c];
+    }
+}
+
+// x split into its TF32 part and the FP32 rest.
+__device__ __forceinline__ void split_tf32(float x, float &hi, float &lo)
+{
+    hi = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+    lo = x - hi;
+}
+
+// K runs along the rows (`along_rows` = 0: A, or column-major B, K is the
+// contiguous dimension) or down the columns (1: row-major B, K counts rows).
+// Part p of 3 of the output holds hi, hi, lo (first = 0: A) or hi, lo, hi
+// (first = 1: B), so the K-concatenated product pairs hi(A) with hi(B) and
+// lo(B), and lo(A) with hi(B).  One thread per input element, rows walked by
+// CTAs, columns by threads (coalesced reads and writes).
+__global__ void __launch_bounds__(256) split3_kernel(const float *__restrict__ src, long long lds,
+                                                     float *__restrict__ dst, long long ldd, long long rows,
+                                                     long long cols, int along_rows, int b_side)
+{
+    for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
+        const float *sr = src + r * lds;
+        for (long long c = threadIdx.x; c < cols; c += blockDim.x) {
+            float hi, lo;
+            split_tf32(sr[c], hi, lo);
+            const float p0 = hi, p1 = b_side ? lo : hi, p2 = b_side ? hi : lo;
+            if (along_rows) {  // K = rows: parts are row blocks
+                dst[r * ldd + c] = p0;
+                dst[(r + rows) * ldd + c] = p1;
+                dst[(r + 2 * rows) * ldd + c] = p2;
+            } else {  // K = cols: parts are column blocks of one row
+                float *dr = dst + r * ldd;
+                dr[c] = p0;
+                dr[c + cols] = p1;
+                dr[c + 2 * cols] = p2;
+            }
+        }
     }
 }
 
@@ -95,6 +138,15 @@ cudaError_t launch_repack(const void *src, int64_t lds, void *dst, int64_t ldd, 
     else
         repack_rows_kernel<uint16_t><<<grid, 256, 0, stream>>>(
             static_cast<const uint16_t *>(src), lds, static_cast<uint16_t *>(dst), ldd, rows, cols);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_split3(const float *src, int64_t lds, float *dst, int64_t ldd, int64_t rows, int64_t cols,
+                          bool along_rows, bool b_side, int sm_count, cudaStream_t stream)
+{
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    split3_kernel<<<rows_grid(rows, sm_count), 256, 0, stream>>>(src, lds, dst, ldd, rows, cols, along_rows ? 1 : 0,
+                                                                 b_side ? 1 : 0);
     return cudaGetLastError();
 }
 

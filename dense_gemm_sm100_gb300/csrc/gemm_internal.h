@@ -132,6 +132,16 @@ cudaError_t launch_tile_split_reduce(const float *partials, int splits, int64_t 
 cudaError_t launch_repack(const void *src, int64_t lds, void *dst, int64_t ldd, int64_t rows,
                           int64_t cols, int elem_bytes, int sm_count, cudaStream_t stream);
 
+// Three-part TF32 split of an FP32 operand (rows x cols at pitch lds) for the
+// FP32-accurate tensor-core mode: x = hi + lo, hi = x with its low 13
+// mantissa bits cleared, lo = x - hi.  along_rows = false (A, or column-major
+// B: K is the column index): dst row r = [p0 | p1 | p2], 3*cols wide;
+// along_rows = true (row-major B: K is the row index): dst rows r, r + rows,
+// r + 2*rows = p0, p1, p2.  (p0, p1, p2) = (hi, hi, lo) for A, (hi, lo, hi)
+// for B (b_side), so A3 B3 = hi(A)hi(B) + hi(A)lo(B) + lo(A)hi(B).
+cudaError_t launch_split3(const float *src, int64_t lds, float *dst, int64_t ldd, int64_t rows, int64_t cols,
+                          bool along_rows, bool b_side, int sm_count, cudaStream_t stream);
+
 // C[i*ldc + j] = 0 for i < M, j < N.
 cudaError_t launch_zero_fill(float *C, int64_t ldc, int64_t M, int64_t N, int sm_count,
                              cudaStream_t stream);

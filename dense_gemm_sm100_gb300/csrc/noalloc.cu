@@ -105,6 +105,7 @@ extern "C" int gemm_run_noalloc(int layout_b, int64_t M, int64_t N, int64_t K, c
 {
     int rc = gemm_validate(layout_b, M, N, K, A, lda, B, ldb, C, ldc, dtype);
     if (rc != GEMM_OK) return rc;
+    if (dtype == GEMM_F32_3XTF32) return GEMM_ERR_INVALID;  // its split operands need a workspace
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         cudaGetLastError();

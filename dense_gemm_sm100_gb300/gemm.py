@@ -25,6 +25,7 @@ GEMM_B_COL_MAJOR = 1
 GEMM_F32 = 0
 GEMM_TF32 = 1
 GEMM_BF16 = 2
+GEMM_F32_3XTF32 = 3
 
 GEMM_OK = 0
 GEMM_ERR_INVALID = -1
@@ -48,7 +49,7 @@ GEMM_OPT_ELEMENTWISE = 11
 GEMM_OPT_WORKSPACE_LIMIT = 12
 GEMM_OPT_TC_STAGE_SLICES = 13
 
-DTYPES = {"f32": GEMM_F32, "tf32": GEMM_TF32, "bf16": GEMM_BF16}
+DTYPES = {"f32": GEMM_F32, "tf32": GEMM_TF32, "bf16": GEMM_BF16, "f32x3": GEMM_F32_3XTF32}
 LAYOUTS = {"row": GEMM_B_ROW_MAJOR, "col": GEMM_B_COL_MAJOR}
 
 LIB_PATH = _build.LIB_PATH

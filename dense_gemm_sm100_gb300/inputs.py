@@ -31,6 +31,7 @@ B_COL_MAJOR = 1
 F32 = "f32"
 TF32 = "tf32"
 BF16 = "bf16"
+F32X3 = "f32x3"  # FP32 operands, FP32-accurate product on the tensor cores
 
 
 @dataclass(frozen=True)
@@ -77,7 +78,14 @@ PROFILE_WORKLOADS = {
     "ffn_tf32_4096x7168x4096": Workload("ffn_tf32_4096x7168x4096", 4096, 7168, 4096,
                                         B_ROW_MAJOR, "normal", 4, 0.02, TF32),
 }
-ALL_WORKLOADS = {**WORKLOADS, **PROFILE_WORKLOADS}
+# The 8192^3 FP32 operands (same draws as fp32_8192_row) in the FP32-accurate
+# tensor-core mode: an extra, labelled mode, not one of the specified configs.
+EXTRA_WORKLOADS = {
+    "fp32x3_8192_row": Workload("fp32x3_8192_row", 8192, 8192, 8192, B_ROW_MAJOR, "uniform", 3,
+                                dtype=F32X3),
+}
+
+ALL_WORKLOADS = {**WORKLOADS, **PROFILE_WORKLOADS, **EXTRA_WORKLOADS}
 
 
 def _draw(gen: torch.Generator, shape, dist: str, sigma: float) -> torch.Tensor:
@@ -103,7 +111,8 @@ def make_operands(M: int, N: int, K: int, *, layout_b: int = B_ROW_MAJOR,
     """Return ``(A, B)`` as CPU tensors in the storage the ABI expects.
 
     A is (M, K) row-major; B is (K, N) for row-major or (N, K) for
-    column-major.  Both are float32, or bfloat16 when ``dtype == "bf16"``.
+    column-major.  Both are float32 (``f32``, ``tf32``, ``f32x3``), or bfloat16
+    when ``dtype == "bf16"``.
     """
     gen = torch.Generator(device="cpu").manual_seed(int(seed))
     A = _draw(gen, (M, K), dist, sigma)
@@ -111,7 +120,7 @@ def make_operands(M: int, N: int, K: int, *, layout_b: int = B_ROW_MAJOR,
     if dtype == BF16:
         A = A.to(torch.bfloat16)
         B = B.to(torch.bfloat16)
-    elif dtype not in (F32, TF32):
+    elif dtype not in (F32, TF32, F32X3):
         raise ValueError(f"unknown dtype {dtype!r}")
     return A.contiguous(), store_b(B, layout_b)
 

@@ -32,6 +32,13 @@
  *              products accumulate in FP32.
  *   GEMM_BF16  A, B bfloat16 (uint16 bit patterns), C float.  Tensor cores
  *              (tcgen05.mma kind::f16 with BF16 inputs), FP32 accumulation.
+ *   GEMM_F32_3XTF32  A, B, C float; FP32-level accuracy on the tensor cores.
+ *              Each operand is split into a TF32 part and the FP32 rest
+ *              (x = hi + lo) in the workspace, three times along K, and one
+ *              TF32 product over 3K computes hi(A)hi(B) + hi(A)lo(B) +
+ *              lo(A)hi(B): A·B up to the lo(A)lo(B) term, about 2^-22 of
+ *              |a·b|, within the FP32 mode's error bound.  Needs 3 (M + N) K
+ *              floats of workspace; finite inputs (an infinity gives NaN).
  *
  * Ownership and threading: the caller owns A, B, C and the stream.  A handle
  * owns a small device status word and a device workspace that grows on
@@ -65,6 +72,7 @@ extern "C" {
 #define GEMM_F32 0
 #define GEMM_TF32 1
 #define GEMM_BF16 2
+#define GEMM_F32_3XTF32 3
 
 /* Return codes. */
 #define GEMM_OK 0

@@ -61,7 +61,8 @@ P = 0x10000  # a fake, 16-byte aligned address: gemm_validate never dereferences
     ((0, 4, 4, 4, P, 4, P, 4, P, 4, 0), 0),
     ((1, 4, 4, 4, P, 4, P, 4, P, 4, 2), 0),
     ((2, 4, 4, 4, P, 4, P, 4, P, 4, 0), -1),      # bad layout
-    ((0, 4, 4, 4, P, 4, P, 4, P, 4, 3), -1),      # bad dtype
+    ((0, 4, 4, 4, P, 4, P, 4, P, 4, 4), -1),      # bad dtype
+    ((0, 4, 4, 4, P, 4, P, 4, P, 4, 3), 0),       # FP32-accurate tensor-core mode
     ((0, -1, 4, 4, P, 4, P, 4, P, 4, 0), -1),     # negative M
     ((0, 4, 4, 4, P, 3, P, 4, P, 4, 0), -1),      # lda < K
     ((0, 4, 5, 4, P, 4, P, 4, P, 5, 0), -1),      # row-major ldb < N
