@@ -226,7 +226,8 @@ int gemm_version(void);
  * array on every GPU that loads it, until the process exits.  When the
  * re-packed A and B together need more than that, the call returns
  * GEMM_ERR_INVALID and launches nothing (aligned operands need no scratch and
- * have no such limit).
+ * have no such limit).  GEMM_F32_3XTF32, whose split operands always need
+ * workspace, is refused the same way.
  *
  * The first call on a device does a one-time set-up there (device check,
  * kernel attributes, lookup of the scratch array's device address); make
