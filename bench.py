@@ -46,9 +46,11 @@ NOMINAL_PF = {"bf16": 2.25, "tf32": 1.1, "f32x3": 1.1 / 3}  # f32x3: three TF32 
 # ncu capture of the kernel as it is now; None until captured for this version.
 # Key: workload name -> (bytes per launch, summary file under profiles/).
 NCU_TRAFFIC: dict[str, tuple[float, str]] = {
-    "fp32_8192_row": (2714.7e6 + 260.4e6, "profiles/dram_traffic_full_size.md"),
-    "ffn_bf16_8192x14336x4096": (481.4e6 + 434.8e6, "profiles/dram_traffic_full_size.md"),
-    "ffn_tf32_8192x14336x4096": (2202.0e6 + 454.1e6, "profiles/dram_traffic_full_size.md"),
+    "fp32_8192_row": (2714.6e6 + 260.8e6, "profiles/dram_traffic_full_size.md"),
+    "ffn_bf16_8192x14336x4096": (483.6e6 + 433.7e6, "profiles/dram_traffic_full_size.md"),
+    "ffn_tf32_8192x14336x4096": (1817.0e6 + 446.0e6, "profiles/dram_traffic_full_size.md"),
+    # the dominant kernel of the mode: the TF32 product over 3K
+    "fp32x3_8192_row": (8557.0e6 + 259.2e6, "profiles/dram_traffic_full_size.md"),
 }
 
 DESCRIPTIONS = {
