@@ -97,3 +97,22 @@ def test_ncu_summary_table_from_raw_csv():
     assert "| registers / thread | 128 register/thread |" in lines
     assert not any(l.startswith("| tensor pipe") for l in lines)  # not in the report
     assert lines[-1].startswith("| top stalls per issued instruction (sgemm_simt_kernel) | math_pipe_throttle 2.10, wait 1.13")
+
+
+def test_tensor_modes_are_described_and_peaked():
+    """Every tensor-core mode the benchmark runs is a known workload with a
+    description, and its peak is the measured BF16 burst scaled by the nominal
+    rate of its input type: TF32 = 1.1/2.25 of BF16, and the FP32-accurate
+    mode (three TF32 products per FP32 product) a third of TF32."""
+    from dense_gemm_sm100_gb300 import inputs
+    peaks = dict(bench.FALLBACK)
+    for name in bench.TC_WORKLOADS:
+        assert name in inputs.ALL_WORKLOADS and name in bench.DESCRIPTIONS
+        assert inputs.ALL_WORKLOADS[name].dtype in bench.NOMINAL_PF
+    bf16 = bench.tensor_peak("bf16", peaks)
+    assert bf16 == peaks["bf16_tflops"]
+    assert abs(bench.tensor_peak("tf32", peaks) - bf16 * 1.1 / 2.25) < 1e-9
+    assert abs(bench.tensor_peak("f32x3", peaks) - bench.tensor_peak("tf32", peaks) / 3) < 1e-9
+    w = inputs.ALL_WORKLOADS["fp32x3_8192_row"]
+    ref = inputs.WORKLOADS["fp32_8192_row"]
+    assert (w.M, w.N, w.K, w.layout_b, w.dist, w.seed) == (ref.M, ref.N, ref.K, ref.layout_b, ref.dist, ref.seed)
