@@ -652,7 +652,7 @@ def main(argv=None):
     ap.add_argument("--simt-config", type=int, default=0,
                     help="force the FP32 tile configuration (GEMM_OPT_SIMT_CONFIG; 0 = chosen per shape)")
     ap.add_argument("--tc-mode", type=int, default=0,
-                    help="force the tensor-core mode (GEMM_OPT_TC_CLUSTER 1..3; 0 = default)")
+                    help="force the tensor-core mode (GEMM_OPT_TC_CLUSTER: 1 one CTA per tile, 3 pair MMA; 0 = default)")
     ap.add_argument("--split-k", type=int, default=0,
                     help="GEMM_OPT_SPLIT_K (0 = chosen per shape, 1 = never, n = n slices)")
     ap.add_argument("--results", default=None,

@@ -38,8 +38,9 @@ def _sources():
 
 
 def _inputs():
+    # every public header (gemm.h, gemm_ladder.h, gemm_peaks.h, ...) is an input
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(
-        os.path.join(CSRC, "*.h")) + [os.path.join(ROOT, "include", "gemm.h"), __file__]
+        os.path.join(CSRC, "*.h")) + sorted(glob.glob(os.path.join(ROOT, "include", "*.h"))) + [__file__]
 
 
 def up_to_date() -> bool:

@@ -20,6 +20,11 @@ struct gemm_ctx {
     int *d_status = nullptr;
     void *ws = nullptr;
     size_t ws_bytes = 0;
+    // Recorded on the caller's stream after every call that used the
+    // workspace; growth waits on it (stream-ordered) before the old buffer
+    // is released.
+    cudaEvent_t ws_event = nullptr;
+    bool ws_event_recorded = false;
     std::string last_error;
     std::string last_path;
     int64_t launches = 0;
@@ -32,7 +37,7 @@ struct gemm_ctx {
     int elementwise = 0;  // FP32 unaligned operands: element-wise producer (1) or re-pack (0)
     size_t ws_limit = 0;  // 0: none; else the workspace never grows beyond this many bytes
     int split_k = 0;      // 0: chosen per shape; 1: never; n > 1: n K slices (FP32 path)
-    int tc_cluster = 3;   // tensor-core mode: 1 one CTA per tile, 2 multicast pairs, 3 pair MMA
+    int tc_cluster = 3;   // tensor-core mode: 1 one CTA per tile, 3 pair MMA
     int tc_tma_store = 1; // tensor-core epilogue writes C with TMA stores when C allows it
     int tc_slices = 0;    // pair MMA: K slices per ring stage (0: library's choice)
     int debug_drop = 0;   // test hook (GEMM_OPT_DEBUG_DROP_LOAD)
@@ -130,7 +135,7 @@ struct PackPlan {
 
 // Tensor-core mode for an M-row problem: the configured CTA-pair mode needs
 // more than one 128-row tile row.
-int tc_cluster_for(const gemm_ctx *h, int64_t M) { return h->tc_cluster >= 2 && M > dg::kTcBM ? h->tc_cluster : 1; }
+int tc_cluster_for(const gemm_ctx *h, int64_t M) { return h->tc_cluster == 3 && M > dg::kTcBM ? 3 : 1; }
 
 PackPlan plan_pack(const gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K,
                    const void *A, int64_t lda, const void *B, int64_t ldb, int dtype)
@@ -149,13 +154,11 @@ PackPlan plan_pack(const gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_
         pp.ldb = round_up(row ? N : K3, 4);
         pp.b_bytes = static_cast<size_t>(round_up((row ? K3 : N) * pp.ldb * 4, 256));
         const int cluster = tc_cluster_for(h, M);
-        if (cluster != 2) {
-            const int64_t ctas = h->max_ctas > 0 ? h->max_ctas : h->sm_count;
-            const int64_t slots = cluster == 3 ? ctas / 2 : ctas;
-            pp.tc_split = dg::tc_pick_splits(dg::tc_units(M, N, cluster), slots, K3, 4, h->split_k);
-            pp.split_bytes = static_cast<size_t>(
-                round_up(static_cast<int64_t>(dg::tc_partial_bytes(M, N, pp.tc_split)), 256));
-        }
+        const int64_t ctas = h->max_ctas > 0 ? h->max_ctas : h->sm_count;
+        const int64_t slots = cluster == 3 ? ctas / 2 : ctas;
+        pp.tc_split = dg::tc_pick_splits(dg::tc_units(M, N, cluster), slots, K3, 4, h->split_k);
+        pp.split_bytes = static_cast<size_t>(
+            round_up(static_cast<int64_t>(dg::tc_partial_bytes(M, N, pp.tc_split)), 256));
         return pp;
     }
     const int es = elem_bytes(dtype);
@@ -191,18 +194,20 @@ PackPlan plan_pack(const gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_
             round_up(static_cast<int64_t>(dg::simt_partial_bytes(pp.simt_config, layout_b, pp.split)), 256));
     } else {
         const int cluster = tc_cluster_for(h, M);
-        if (cluster != 2) {
-            const int64_t ctas = h->max_ctas > 0 ? h->max_ctas : h->sm_count;
-            const int64_t slots = cluster == 3 ? ctas / 2 : ctas;
-            pp.tc_split = dg::tc_pick_splits(dg::tc_units(M, N, cluster), slots, K, es, h->split_k);
-            pp.split_bytes = static_cast<size_t>(
-                round_up(static_cast<int64_t>(dg::tc_partial_bytes(M, N, pp.tc_split)), 256));
-        }
+        const int64_t ctas = h->max_ctas > 0 ? h->max_ctas : h->sm_count;
+        const int64_t slots = cluster == 3 ? ctas / 2 : ctas;
+        pp.tc_split = dg::tc_pick_splits(dg::tc_units(M, N, cluster), slots, K, es, h->split_k);
+        pp.split_bytes = static_cast<size_t>(
+            round_up(static_cast<int64_t>(dg::tc_partial_bytes(M, N, pp.tc_split)), 256));
     }
     return pp;
 }
 
-int ensure_workspace(gemm_ctx *h, size_t need)
+// Grows the workspace in stream order on `stream`: the stream first waits
+// for the last call that used the old buffer, then frees it and allocates
+// the new one from the device's stream-ordered pool.  Nothing waits on the
+// host, and work the caller queued on other streams is not held up.
+int ensure_workspace(gemm_ctx *h, size_t need, cudaStream_t stream)
 {
     if (need <= h->ws_bytes) return GEMM_OK;
     if (h->ws_limit > 0 && need > h->ws_limit) {
@@ -215,19 +220,33 @@ int ensure_workspace(gemm_ctx *h, size_t need)
     size_t bytes = need > grow ? need : grow;
     bytes = (bytes + (size_t{2} << 20) - 1) & ~((size_t{2} << 20) - 1);
     if (h->ws_limit > 0 && bytes > h->ws_limit) bytes = need;  // stay within the limit
-    // Earlier queued work may still read the old buffer.
-    cudaError_t e = cudaDeviceSynchronize();
-    if (e != cudaSuccess) return cuda_fail(h, e, "cudaDeviceSynchronize before workspace growth");
-    if (h->ws) cudaFree(h->ws);
+    cudaError_t e = cudaSuccess;
+    if (h->ws) {
+        // Earlier calls (on this or another stream) may still read the old buffer.
+        if (h->ws_event_recorded) e = cudaStreamWaitEvent(stream, h->ws_event, 0);
+        if (e == cudaSuccess) e = cudaFreeAsync(h->ws, stream);
+        if (e != cudaSuccess) return cuda_fail(h, e, "stream-ordered release of the old workspace");
+    }
     h->ws = nullptr;
     h->ws_bytes = 0;
-    e = cudaMalloc(&h->ws, bytes);
+    h->ws_event_recorded = false;
+    e = cudaMallocAsync(&h->ws, bytes, stream);
     if (e != cudaSuccess) {
         h->ws = nullptr;
         cudaGetLastError();
-        return fail(h, GEMM_ERR_NOMEM, std::string("workspace cudaMalloc: ") + cudaGetErrorString(e));
+        return fail(h, GEMM_ERR_NOMEM, std::string("workspace cudaMallocAsync: ") + cudaGetErrorString(e));
     }
     h->ws_bytes = bytes;
+    return GEMM_OK;
+}
+
+// After a call whose launches read or write the workspace: its end on
+// `stream` is what the next growth waits for.
+int note_workspace_use(gemm_ctx *h, cudaStream_t stream)
+{
+    cudaError_t e = cudaEventRecord(h->ws_event, stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "workspace-use event");
+    h->ws_event_recorded = true;
     return GEMM_OK;
 }
 
@@ -408,7 +427,7 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
         const int cluster = tc_cluster_for(h, M);
         // MN-major B; 32-bit elements need 32-byte swizzle atoms there.
         const CUtensorMapSwizzle b_swz = es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B;
-        const bool b_chunks = layout_b == GEMM_B_ROW_MAJOR && cluster != 2 && N % (128 / es) == 0;
+        const bool b_chunks = layout_b == GEMM_B_ROW_MAJOR && N % (128 / es) == 0;
         if (b_chunks)
             rc = encode_b_chunks(h, &tmB, es, B, N, K, ldb, bk, (cluster == 3 ? dg::kTcBN / 2 : dg::kTcBN) / (128 / es),
                                  b_swz);
@@ -435,7 +454,6 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
         if (e != cudaSuccess) return cuda_fail(h, e, "tensor-core kernel launch");
         path = std::string(split3 ? "f32x3_tc_tf32" : dtype == GEMM_BF16 ? "tc_bf16" : "tc_tf32") +
                (cluster == 3 ? (wide ? "_pair256x256w_" : "_pair256x256_") : "_128x256_") + lay +
-               (cluster == 2 ? "_cluster2" : "") +
                (b_chunks ? "+b3d" : "") + path;
         if (sp.splits > 1) {
             ++h->launches;
@@ -497,9 +515,11 @@ int gemm_create(gemm_handle_t *out, int device)
     if (e == cudaSuccess) e = dg::prepare_tc();
     if (e == cudaSuccess) e = cudaMalloc(&h->d_status, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(int));
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ws_event, cudaEventDisableTiming);
     if (e != cudaSuccess) {
         cudaGetLastError();
         if (h->d_status) cudaFree(h->d_status);
+        if (h->ws_event) cudaEventDestroy(h->ws_event);
         delete h;
         return GEMM_ERR_CUDA;
     }
@@ -513,8 +533,12 @@ int gemm_destroy(gemm_handle_t h)
     {
         DeviceGuard guard(h->device);
         cudaDeviceSynchronize();
-        if (h->ws) cudaFree(h->ws);
+        if (h->ws) {
+            cudaFreeAsync(h->ws, nullptr);  // allocated from the stream-ordered pool
+            cudaStreamSynchronize(nullptr);
+        }
         if (h->d_status) cudaFree(h->d_status);
+        if (h->ws_event) cudaEventDestroy(h->ws_event);
         if (h->copy_in) cudaStreamDestroy(h->copy_in);
         if (h->copy_out) cudaStreamDestroy(h->copy_out);
         for (cudaEvent_t ev : {h->ev_start, h->ev_done})
@@ -547,10 +571,12 @@ int gemm_run(gemm_handle_t h, int layout_b, int64_t M, int64_t N, int64_t K, con
     DeviceGuard guard(h->device);
     const PackPlan pp = plan_pack(h, layout_b, M, N, K, A, lda, B, ldb, dtype);
     if (pp.total()) {
-        rc = ensure_workspace(h, pp.total());
+        rc = ensure_workspace(h, pp.total(), stream);
         if (rc) return rc;
     }
-    return run_device(h, layout_b, M, N, K, A, lda, B, ldb, C, ldc, dtype, stream, pp, 0);
+    rc = run_device(h, layout_b, M, N, K, A, lda, B, ldb, C, ldc, dtype, stream, pp, 0);
+    if (rc == GEMM_OK && pp.total()) rc = note_workspace_use(h, stream);
+    return rc;
 }
 
 namespace {
@@ -606,7 +632,7 @@ void tile_shape(const gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K
         *full_slots = int64_t{h->sm_count} * t.ctas_per_sm;
         *slots = h->max_ctas > 0 ? h->max_ctas : *full_slots;
     } else {
-        const bool pair = h->tc_cluster >= 2;
+        const bool pair = h->tc_cluster == 3;
         const int64_t ctas = h->max_ctas > 0 ? h->max_ctas : h->sm_count;
         *bm = pair ? 2 * dg::kTcBM : dg::kTcBM;  // a pair covers two tile rows
         *bn = dg::kTcBN;
@@ -729,7 +755,7 @@ int gemm_run_host(gemm_handle_t h, int layout_b, int64_t M, int64_t N, int64_t K
     for (int64_t mi : {block_m(0), block_m(hb.pm - 1)})
         for (int64_t nj : {block_n(0), block_n(hb.pn - 1), N})
             extra = std::max(extra, plan_pack(h, layout_b, mi, nj, K, nullptr, lda_d, nullptr, ldb_d, dtype).total());
-    rc = ensure_workspace(h, staged + extra);
+    rc = ensure_workspace(h, staged + extra, stream);
     if (rc) return rc;
     uint8_t *ws = static_cast<uint8_t *>(h->ws);
     uint8_t *A_d = ws, *B_d = ws + a_bytes;
@@ -804,6 +830,7 @@ int gemm_run_host(gemm_handle_t h, int layout_b, int64_t M, int64_t N, int64_t K
     e = cudaEventRecord(h->ev_done, h->copy_out);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, h->ev_done, 0);  // the call ends on `stream`
     if (e != cudaSuccess) return cuda_fail(h, e, "host-copy pipeline completion");
+    if ((rc = note_workspace_use(h, stream))) return rc;
     h->last_path = "host+" + path;
     if (block > 1) h->last_path += "+blocks" + std::to_string(hb.pm) + "x" + std::to_string(hb.pn);  // launches: (pm-1)*pn+1
     return GEMM_OK;
@@ -873,7 +900,7 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value)
         h->tc_tma_store = static_cast<int>(value);
         return GEMM_OK;
     case GEMM_OPT_TC_CLUSTER:
-        if (value < 1 || value > 3) break;
+        if (value != 1 && value != 3) break;
         h->tc_cluster = static_cast<int>(value);
         return GEMM_OK;
     case GEMM_OPT_TC_STAGE_SLICES:

@@ -87,9 +87,9 @@ cudaError_t launch_simt_tail_reduce(int config, int layout_b, int M, int N, int 
 
 // Tensor-core GEMM; dtype is GEMM_TF32 or GEMM_BF16.  tmA/tmB as above.
 // tmC (may be null): C as FP32 dims {N, M}, box {32, 32}, 128-byte swizzle,
-// used for TMA stores; null means per-thread stores.  cluster = 2 runs CTA
-// pairs that share (multicast) the B tile; cluster = 3 runs the pair MMA
-// (cta_group::2, 256x256 per pair); lc.grid must then be even.
+// used for TMA stores; null means per-thread stores.  cluster = 1 runs one
+// CTA per 128x256 tile; cluster = 3 runs the pair MMA (cta_group::2, 256x256
+// per pair of CTAs); lc.grid must then be even.
 constexpr int kTcBoxC = 32;
 // K split of the tensor-core kernels (modes 1 and 3): every tile unit is cut
 // into `splits` slices of kt_per_split stages; slice s of tile (mb, nb) goes

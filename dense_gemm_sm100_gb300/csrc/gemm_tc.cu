@@ -19,12 +19,6 @@
 //    takes guarded per-thread stores instead.
 //  * persistent grid walking tiles in groups of `group_m` tile rows for L2
 //    reuse ("GEMM 性能优化", Wave 模型与 L2 命中率).
-//  * CL = 2: CTAs run in clusters of two that own vertically adjacent tiles
-//    (same B columns).  Each CTA loads its own A and one half of the shared B
-//    tile, multicast into both CTAs' shared memory, so every SM reads 32 KB
-//    instead of 48 KB from L2 per stage (data reuse one level further out
-//    than the pages' shared-memory tiling).  Each MMA's commit releases the
-//    ring slot in both CTAs.
 // A is K-major.  B is K-major when stored column-major (the corner-turning
 // case of "PMPP Chapter 06: Performance considerations", section 1) and
 // MN-major when stored row-major; the shared-memory descriptor says which,
@@ -120,9 +114,9 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t fmt, uint32_t b_mn_ma
            (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
 }
 
-// DT: 0 = BF16 (2-byte elements), 1 = TF32 (4-byte elements).  CL: CTAs per
-// cluster sharing the B tile (1 or 2).
-template <int DT, int LAYOUT_B, int CL>
+// DT: 0 = BF16 (2-byte elements), 1 = TF32 (4-byte elements).  One CTA per
+// 128 x 256 tile.
+template <int DT, int LAYOUT_B>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB,
@@ -142,7 +136,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     // the descriptor is 4 x 128 bytes instead of 8 x 128 bytes.
     constexpr uint32_t B_MN_LAYOUT = DT == 0 ? kLayoutSw128 : kLayoutSw128Atom32;
     constexpr uint32_t B_MN_SBO = DT == 0 ? 1024u : 512u;
-    constexpr uint16_t CLUSTER_MASK = (1u << CL) - 1u;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -162,17 +155,17 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
-    const int cluster = blockIdx.x / CL;
-    const int clusters = gridDim.x / CL;
-    const int base_units = ((p.tiles_m + CL - 1) / CL) * p.tiles_n;
+    const uint32_t rank = 0u;
+    const int cluster = blockIdx.x;
+    const int clusters = gridDim.x;
+    const int base_units = p.tiles_m * p.tiles_n;
     const int num_units = base_units * p.splits;
     const int k_tiles = (p.K + BK - 1) / BK;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar + 8 * s, 1);
-            mbar_init(empty_bar + 8 * s, CL);  // one release per MMA issuer of the cluster
+            mbar_init(empty_bar + 8 * s, 1);  // released by the MMA issuer's commit
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar + 8 * b, 1);
@@ -187,10 +180,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_relinquish();
     }
     tc_fence_before_sync();
-    if (CL > 1)
-        cluster_sync();  // peers' barriers are initialised before anyone targets them
-    else
-        __syncthreads();
+    __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -204,7 +194,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int u = cluster; ok && u < num_units; u += clusters) {
                 const KRange kr = unit_krange(u, p, base_units, k_tiles);
                 int mb, nb;
-                unit_coords<CL>(kr.ub, p, rank, mb, nb);
+                unit_coords<1>(kr.ub, p, rank, mb, nb);
                 for (int kt = kr.kt0; kt < kr.kt1; ++kt, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
@@ -216,34 +206,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t fb = full_bar + 8 * s;
                     const uint32_t a_st = sbase + s * STAGE_BYTES;
                     const uint32_t b_st = a_st + A_BYTES;
-                    // A of this CTA, plus all of B: this CTA's half and (CL = 2)
-                    // the peer's half, which the peer multicasts here.
                     mbar_arrive_expect_tx(fb, STAGE_BYTES);
                     if (p.debug_drop && blockIdx.x == 0 && it == 0) continue;  // bytes that never come
                     tma_load_2d(a_st, &tmA, fb, kt * BK, mb * BM);
                     if (LAYOUT_B == 0) {
-                        if (CL == 1 && p.b_chunks) {
+                        if (p.b_chunks) {
                             tma_load_3d(b_st, &tmB, fb, 0, kt * BK, nb * BN / BOX_N);  // all B_BOXES chunks
-                        } else if (CL == 1) {
+                        } else {
 #pragma unroll
                             for (int j = 0; j < B_BOXES; ++j)
                                 tma_load_2d(b_st + j * BOX_BYTES, &tmB, fb, nb * BN + j * BOX_N, kt * BK);
-                        } else {
-#pragma unroll
-                            for (int jj = 0; jj < B_BOXES / 2; ++jj) {
-                                const int j = static_cast<int>(rank) * (B_BOXES / 2) + jj;
-                                tma_load_2d_multicast(b_st + j * BOX_BYTES, &tmB, fb, nb * BN + j * BOX_N,
-                                                      kt * BK, CLUSTER_MASK);
-                            }
                         }
                     } else {
-                        if (CL == 1) {
-                            tma_load_2d(b_st, &tmB, fb, kt * BK, nb * BN);
-                            tma_load_2d(b_st + B_BYTES / 2, &tmB, fb, kt * BK, nb * BN + BN / 2);
-                        } else {
-                            tma_load_2d_multicast(b_st + rank * (B_BYTES / 2), &tmB, fb, kt * BK,
-                                                  nb * BN + static_cast<int>(rank) * (BN / 2), CLUSTER_MASK);
-                        }
+                        tma_load_2d(b_st, &tmB, fb, kt * BK, nb * BN);
+                        tma_load_2d(b_st + B_BYTES / 2, &tmB, fb, kt * BK, nb * BN + BN / 2);
                     }
                 }
             }
@@ -255,13 +231,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                     mbar_wait(full_bar + 8 * (i % STAGES), (i / STAGES) & 1u, &dummy, nullptr,
                               kWaitDrain, p.timeout_ns);
                 }
-            } else if (CL > 1) {
-                // Every release of the last stages (this CTA's MMA and the
-                // peer's) must have landed before shared memory goes away.
-                const uint32_t n = it < (uint32_t)STAGES ? it : (uint32_t)STAGES;
-                for (uint32_t i = it - n; i < it; ++i)
-                    mbar_wait(empty_bar + 8 * (i % STAGES), (i / STAGES) & 1u, abort_flag, p.status,
-                              kWaitDrain, p.timeout_ns);
             }
         }
     } else if (warp == 1) {
@@ -308,10 +277,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             else
                                 tc_mma_tf32(d_tmem, ad[kk], bd[kk], IDESC, kk > 0 ? 1u : acc0);
                         }
-                        if (CL == 1)
-                            tc_commit(empty_bar + 8 * s);
-                        else
-                            tc_commit_multicast(empty_bar + 8 * s, CLUSTER_MASK);
+                        tc_commit(empty_bar + 8 * s);
                     }
                     __syncwarp();
                     issued = true;
@@ -337,7 +303,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int u = cluster; u < num_units; u += clusters, ++acc_it) {
             const KRange kr = unit_krange(u, p, base_units, k_tiles);
             int mb, nb;
-            unit_coords<CL>(kr.ub, p, rank, mb, nb);
+            unit_coords<1>(kr.ub, p, rank, mb, nb);
             const uint32_t abuf = acc_it & 1u;
             const uint32_t aph = (acc_it >> 1) & 1u;
             bool ok = true;
@@ -416,10 +382,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     tc_fence_before_sync();
     __syncwarp();
-    if (CL > 1)
-        cluster_sync();  // no CTA leaves while its peer may still target its shared memory
-    else
-        __syncthreads();
+    __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, TMEM_COLS);
@@ -782,34 +745,18 @@ cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
     return cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<DT, L, SUB>, tmA, tmB, tmC, p);
 }
 
-template <int DT, int L, int CL>
+template <int DT, int L>
 cudaError_t set_attrs()
 {
-    return cudaFuncSetAttribute(gemm_tc_kernel<DT, L, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                SMEM_BYTES);
+    return cudaFuncSetAttribute(gemm_tc_kernel<DT, L>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
 }
 
-template <int DT, int L, int CL>
+template <int DT, int L>
 cudaError_t launch_one(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                        const TcParams &p, int grid, cudaStream_t stream)
 {
-    if (CL == 1) {
-        gemm_tc_kernel<DT, L, 1><<<grid, THREADS, SMEM_BYTES, stream>>>(tmA, tmB, tmC, p);
-        return cudaGetLastError();
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CL;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<DT, L, CL>, tmA, tmB, tmC, p);
+    gemm_tc_kernel<DT, L><<<grid, THREADS, SMEM_BYTES, stream>>>(tmA, tmB, tmC, p);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -817,8 +764,7 @@ cudaError_t launch_one(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUt
 cudaError_t prepare_tc()
 {
     cudaError_t e = cudaSuccess;
-    cudaError_t (*fns[])() = {set_attrs<0, 0, 1>, set_attrs<0, 1, 1>, set_attrs<1, 0, 1>, set_attrs<1, 1, 1>,
-                              set_attrs<0, 0, 2>, set_attrs<0, 1, 2>, set_attrs<1, 0, 2>, set_attrs<1, 1, 2>,
+    cudaError_t (*fns[])() = {set_attrs<0, 0>, set_attrs<0, 1>, set_attrs<1, 0>, set_attrs<1, 1>,
                               set_pair_attrs<0, 0, 1>, set_pair_attrs<0, 1, 1>, set_pair_attrs<1, 0, 1>,
                               set_pair_attrs<1, 1, 1>, set_pair_attrs<0, 0, 2>, set_pair_attrs<0, 1, 2>,
                               set_pair_attrs<1, 0, 2>, set_pair_attrs<1, 1, 2>};
@@ -830,13 +776,13 @@ cudaError_t prepare_tc()
 int64_t tc_units(int64_t M, int64_t N, int cluster)
 {
     const int64_t tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
-    const int cl = cluster >= 2 ? 2 : 1;
+    const int cl = cluster == 3 ? 2 : 1;
     return ((tiles_m + cl - 1) / cl) * tiles_n;
 }
 
 int tc_grid(int64_t M, int64_t N, int sm_count, int cluster, int splits)
 {
-    const int cl = cluster >= 2 ? 2 : 1;
+    const int cl = cluster == 3 ? 2 : 1;
     const int64_t units = tc_units(M, N, cluster) * (splits > 1 ? splits : 1);
     const int64_t clusters = sm_count >= cl ? sm_count / cl : 1;
     return static_cast<int>(cl * (units < clusters ? units : clusters));
@@ -885,13 +831,13 @@ cudaError_t launch_tc(int dtype, int layout_b, const CUtensorMap &tmA, const CUt
     p.K = K;
     p.tiles_m = (M + BM - 1) / BM;
     p.tiles_n = (N + BN - 1) / BN;
-    const int cl = cluster == 2 ? 2 : cluster == 3 ? 3 : 1;
-    // group_m counts units (tile rows, or tile-row pairs for clusters) along M.
+    const int cl = cluster == 3 ? 3 : 1;
+    // group_m counts units (tile rows, or tile-row pairs for CTA pairs) along M.
     // Pair MMA: the largest group whose A panel (group x 256 rows x K) stays
     // within 32 MB, a quarter of L2, so it is read from DRAM once while the
     // group sweeps the columns of B ("GEMM 性能优化", Wave 模型与 L2 命中率);
     // 16 for BF16 and 8 for TF32 at K = 4096 (measured best, FFN shape).
-    int dflt = cl >= 2 ? 8 : 16;
+    int dflt = 16;
     if (cl == 3) {
         const int64_t panel = int64_t{2 * BM} * K * (dtype == GEMM_BF16 ? 2 : 4);
         const int64_t fit = panel > 0 ? (int64_t{32} << 20) / panel : 16;
@@ -904,9 +850,9 @@ cudaError_t launch_tc(int dtype, int layout_b, const CUtensorMap &tmA, const CUt
     p.timeout_ns = lc.timeout_ns;
     p.c_vec4 = c_vec4 ? 1 : 0;
     p.c_tma = tmC != nullptr ? 1 : 0;
-    p.b_chunks = b_chunks && (cluster == 3 || cluster == 1) && layout_b == 0 ? 1 : 0;
+    p.b_chunks = b_chunks && layout_b == 0 ? 1 : 0;
     p.debug_drop = lc.debug_drop;
-    const bool split = sp.splits > 1 && cluster != 2;
+    const bool split = sp.splits > 1;
     wide = wide && !split;
     p.splits = split ? sp.splits : 1;
     p.kt_per_split = split ? sp.kt_per_split : (K + (128 / (dtype == GEMM_BF16 ? 2 : 4)) - 1) / (128 / (dtype == GEMM_BF16 ? 2 : 4));
@@ -931,16 +877,10 @@ cudaError_t launch_tc(int dtype, int layout_b, const CUtensorMap &tmA, const CUt
         return layout_b == 0 ? launch_pair<1, 0, 1>(tmA, tmB, tc, p, lc.grid, lc.stream)
                              : launch_pair<1, 1, 1>(tmA, tmB, tc, p, lc.grid, lc.stream);
     }
-    if (cl == 1) {
-        if (bf16) return layout_b == 0 ? launch_one<0, 0, 1>(tmA, tmB, tc, p, lc.grid, lc.stream)
-                                       : launch_one<0, 1, 1>(tmA, tmB, tc, p, lc.grid, lc.stream);
-        return layout_b == 0 ? launch_one<1, 0, 1>(tmA, tmB, tc, p, lc.grid, lc.stream)
-                             : launch_one<1, 1, 1>(tmA, tmB, tc, p, lc.grid, lc.stream);
-    }
-    if (bf16) return layout_b == 0 ? launch_one<0, 0, 2>(tmA, tmB, tc, p, lc.grid, lc.stream)
-                                   : launch_one<0, 1, 2>(tmA, tmB, tc, p, lc.grid, lc.stream);
-    return layout_b == 0 ? launch_one<1, 0, 2>(tmA, tmB, tc, p, lc.grid, lc.stream)
-                         : launch_one<1, 1, 2>(tmA, tmB, tc, p, lc.grid, lc.stream);
+    if (bf16) return layout_b == 0 ? launch_one<0, 0>(tmA, tmB, tc, p, lc.grid, lc.stream)
+                                   : launch_one<0, 1>(tmA, tmB, tc, p, lc.grid, lc.stream);
+    return layout_b == 0 ? launch_one<1, 0>(tmA, tmB, tc, p, lc.grid, lc.stream)
+                         : launch_one<1, 1>(tmA, tmB, tc, p, lc.grid, lc.stream);
 }
 
 }  // namespace dg

@@ -14,6 +14,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -25,6 +26,15 @@ namespace {
 // The scratch for re-packed A and B (GEMM_NOALLOC_SCRATCH_BYTES).
 static __device__ __align__(256) unsigned char g_noalloc_scratch[GEMM_NOALLOC_SCRATCH_BYTES];
 
+// Status word of these calls on this device: a kernel whose in-kernel wait
+// expires writes its code here, as a handle's kernels write the handle's
+// status word; gemm_noalloc_sync_status reads and clears it.  Zero at load.
+static __device__ int g_noalloc_status;
+
+// Process-wide settings of these calls (gemm_noalloc_set_option).
+std::atomic<uint64_t> g_timeout_ns{4000000000ull};
+std::atomic<int> g_debug_drop{0};
+
 constexpr int kMaxDevices = 64;
 
 struct DeviceSetup {
@@ -32,6 +42,7 @@ struct DeviceSetup {
     int rc = GEMM_OK;
     int sm_count = 0;
     void *scratch = nullptr;  // device address of g_noalloc_scratch on this device
+    int *status = nullptr;    // device address of g_noalloc_status on this device
 };
 
 std::mutex g_setup_mutex;
@@ -40,7 +51,7 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode_fn = nullptr;
 
 // Once per device, with that device current: check the device, raise the
 // kernels' shared-memory limits, find the tensor-map encoder and look up the
-// device address of the scratch array.
+// device addresses of the scratch array and the status word.
 int setup_device(int dev, DeviceSetup **out)
 {
     std::lock_guard<std::mutex> lock(g_setup_mutex);
@@ -66,9 +77,11 @@ int setup_device(int dev, DeviceSetup **out)
             if (e == cudaSuccess) e = dg::prepare_simt();
             if (e == cudaSuccess) e = dg::prepare_tc();
             if (e == cudaSuccess) e = cudaGetSymbolAddress(&s.scratch, g_noalloc_scratch);
+            if (e == cudaSuccess) e = cudaGetSymbolAddress(reinterpret_cast<void **>(&s.status), g_noalloc_status);
             if (e != cudaSuccess) {
                 cudaGetLastError();
                 s.scratch = nullptr;
+                s.status = nullptr;
                 s.rc = GEMM_ERR_CUDA;
             }
         }
@@ -78,6 +91,16 @@ int setup_device(int dev, DeviceSetup **out)
 }
 
 int64_t up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+int current_device_setup(DeviceSetup **out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return GEMM_ERR_DEVICE;
+    }
+    return setup_device(dev, out);
+}
 
 bool tma_ok(const void *p, int64_t ld, int es)
 {
@@ -106,13 +129,8 @@ extern "C" int gemm_run_noalloc(int layout_b, int64_t M, int64_t N, int64_t K, c
     int rc = gemm_validate(layout_b, M, N, K, A, lda, B, ldb, C, ldc, dtype);
     if (rc != GEMM_OK) return rc;
     if (dtype == GEMM_F32_3XTF32) return GEMM_ERR_INVALID;  // its split operands need a workspace
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        cudaGetLastError();
-        return GEMM_ERR_DEVICE;
-    }
     DeviceSetup *s = nullptr;
-    rc = setup_device(dev, &s);
+    rc = current_device_setup(&s);
     if (rc != GEMM_OK) return rc;
     if (M == 0 || N == 0) return GEMM_OK;
     if (K == 0) {
@@ -150,10 +168,11 @@ extern "C" int gemm_run_noalloc(int layout_b, int64_t M, int64_t N, int64_t K, c
     alignas(64) CUtensorMap tmA;
     alignas(64) CUtensorMap tmB;
     dg::LaunchCommon lc;
-    lc.status = nullptr;  // no status word: an expired wait ends the kernel without a report
-    lc.timeout_ns = 4000000000ull;
+    lc.status = s->status;  // read by gemm_noalloc_sync_status
+    lc.timeout_ns = g_timeout_ns.load();
     lc.group_m = 0;
     lc.stream = stream;
+    lc.debug_drop = g_debug_drop.load();
     const bool c_vec4 = reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 4 == 0;
     cudaError_t e;
     if (dtype == GEMM_F32) {
@@ -182,4 +201,42 @@ extern "C" int gemm_run_noalloc(int layout_b, int64_t M, int64_t N, int64_t K, c
                           static_cast<int>(K), C, ldc, c_vec4, lc, 1, false);
     }
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+extern "C" int gemm_noalloc_sync_status(cudaStream_t stream)
+{
+    DeviceSetup *s = nullptr;
+    int rc = current_device_setup(&s);
+    if (rc != GEMM_OK) return rc;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    int st = 0;
+    if (cudaMemcpy(&st, s->status, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (st == 0) return GEMM_OK;
+    if (cudaMemset(s->status, 0, sizeof st) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_ERR_TIMEOUT;
+}
+
+extern "C" int gemm_noalloc_set_option(int option, int64_t value)
+{
+    switch (option) {
+    case GEMM_OPT_WAIT_TIMEOUT_NS:
+        if (value < 1000000 || value > int64_t{60} * 1000000000) return GEMM_ERR_INVALID;
+        g_timeout_ns.store(static_cast<uint64_t>(value));
+        return GEMM_OK;
+    case GEMM_OPT_DEBUG_DROP_LOAD:
+        if (value != 0 && value != 1) return GEMM_ERR_INVALID;
+        g_debug_drop.store(static_cast<int>(value));
+        return GEMM_OK;
+    default:
+        return GEMM_ERR_INVALID;
+    }
 }

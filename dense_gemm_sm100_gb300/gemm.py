@@ -96,6 +96,8 @@ def load_library():
             "gemm_launch_count": ([vp], i64),
             "gemm_version": ([], ci),
             "gemm_run_noalloc": ([ci, i64, i64, i64, vp, i64, vp, i64, vp, i64, ci, vp], ci),
+            "gemm_noalloc_sync_status": ([vp], ci),
+            "gemm_noalloc_set_option": ([ci, i64], ci),
             "gemm_ladder_run": ([ci, i64, i64, i64, vp, vp, vp, vp], ci),
             "gemm_ladder_name": ([ci], ctypes.c_char_p),
             "gemm_peak_fma_run": ([ci, i64, vp, vp, ctypes.POINTER(ctypes.c_double)], ci),
@@ -170,6 +172,17 @@ def gemm_run_noalloc(layout_b, M, N, K, A, lda, B, ldb, C, ldc, dtype, stream) -
     GEMM_NOALLOC_SCRATCH_BYTES).  For callers that cannot allocate."""
     return load_library().gemm_run_noalloc(layout_b, M, N, K, A, lda, B, ldb, C, ldc, dtype,
                                            stream)
+
+
+def gemm_noalloc_sync_status(stream) -> int:
+    """Waits for `stream`; GEMM_ERR_TIMEOUT if an in-kernel wait of an
+    allocation-free call on the current device expired (then cleared)."""
+    return load_library().gemm_noalloc_sync_status(stream)
+
+
+def gemm_noalloc_set_option(option, value) -> int:
+    """Process-wide wait limit / test hook of the allocation-free calls."""
+    return load_library().gemm_noalloc_set_option(option, value)
 
 
 GEMM_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024

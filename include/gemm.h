@@ -47,6 +47,10 @@
  * problems, and by gemm_run_host).  Calls on one handle must be
  * issued from one host thread at a time and be ordered on the GPU (one
  * stream, or streams the caller orders), because they share the workspace.
+ * Growth is stream-ordered on the calling stream (cudaFreeAsync of the old
+ * buffer after the last call that used it, then cudaMallocAsync from the
+ * device's default memory pool): it neither synchronises the device nor
+ * waits on the host.  gemm_destroy synchronises the device.
  *
  * Errors: every function returns GEMM_OK (0) or a negative GEMM_ERR_* code.
  * Argument errors are detected on the host before anything is launched.
@@ -101,7 +105,7 @@ extern "C" {
  * one wave.  A second kernel adds the slices in slice order.  1 = never.
  * 2..64 = every tile cut into that many slices (fewer if K is short). */
 #define GEMM_OPT_SPLIT_K 7
-#define GEMM_OPT_TC_CLUSTER 8     /* tensor-core mode: 1 one CTA per tile, 2 CTA pairs sharing B by multicast, 3 pair MMA (cta_group::2, default) */
+#define GEMM_OPT_TC_CLUSTER 8     /* tensor-core mode: 1 one CTA per tile, 3 pair MMA (cta_group::2, default); other values are GEMM_ERR_INVALID */
 #define GEMM_OPT_TC_TMA_STORE 9   /* 1 (default): tensor-core epilogue stores C by TMA when aligned */
 /* Test hook for failure detection, 0 by default.  1: in the next runs, CTA 0
  * of the GEMM kernel skips the copies of its first stage while still
@@ -235,15 +239,33 @@ int gemm_version(void);
  * the scratch array and it keeps the last call's contents; nothing in it has
  * to start at zero, because each call writes every element it reads.  Calls
  * that overlap on the GPU (unordered streams, or several host threads) race
- * on the array: order them.  There is no status word: an in-kernel wait that
- * expires ends the kernel without a report (gemm_sync_status covers only
- * handle-based calls).  The call makes no cudaMalloc, cudaFree or other
- * allocating call.
+ * on the array: order them.  An in-kernel wait that expires ends the kernel
+ * with C incomplete and sets a per-device status word (a static device
+ * variable beside the scratch array); gemm_noalloc_sync_status reports it.
+ * The call makes no cudaMalloc, cudaFree or other allocating call.
  */
 #define GEMM_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 int gemm_run_noalloc(int layout_b, int64_t M, int64_t N, int64_t K,
                      const void *A, int64_t lda, const void *B, int64_t ldb,
                      float *C, int64_t ldc, int dtype, cudaStream_t stream);
+
+/*
+ * Status of the allocation-free calls on the current device: waits for
+ * `stream`, then returns GEMM_ERR_TIMEOUT if an in-kernel wait of an earlier
+ * gemm_run_noalloc call on this device expired (C of that call is
+ * incomplete) and clears the report, else GEMM_OK.  The status word is shared
+ * by every allocation-free call on the device, whatever its stream.
+ * Allocates nothing (a 4-byte device-to-host copy).
+ */
+int gemm_noalloc_sync_status(cudaStream_t stream);
+
+/*
+ * Process-wide settings of the allocation-free calls (they have no handle):
+ * GEMM_OPT_WAIT_TIMEOUT_NS (limit of every in-kernel wait, 1e6..6e10 ns,
+ * default 4e9) and the test hook GEMM_OPT_DEBUG_DROP_LOAD (0 or 1, as for a
+ * handle).  Other options are GEMM_ERR_INVALID.  Applies to later calls.
+ */
+int gemm_noalloc_set_option(int option, int64_t value);
 
 #ifdef __cplusplus
 }

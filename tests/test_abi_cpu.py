@@ -153,3 +153,15 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(g, "_lib", None)
     with pytest.raises(g.GemmLibraryMissing):
         g.load_library()
+
+
+def test_noalloc_options_are_checked_on_the_host(lib):
+    """The allocation-free calls' process-wide settings: only the wait limit
+    (1e6..6e10 ns) and the test hook (0/1) exist; nothing touches a GPU."""
+    from dense_gemm_sm100_gb300 import gemm as g
+    assert g.gemm_noalloc_set_option(g.GEMM_OPT_WAIT_TIMEOUT_NS, 999_999) == g.GEMM_ERR_INVALID
+    assert g.gemm_noalloc_set_option(g.GEMM_OPT_WAIT_TIMEOUT_NS, 61_000_000_000) == g.GEMM_ERR_INVALID
+    assert g.gemm_noalloc_set_option(g.GEMM_OPT_DEBUG_DROP_LOAD, 2) == g.GEMM_ERR_INVALID
+    assert g.gemm_noalloc_set_option(g.GEMM_OPT_SIMT_CONFIG, 1) == g.GEMM_ERR_INVALID
+    assert g.gemm_noalloc_set_option(g.GEMM_OPT_WAIT_TIMEOUT_NS, 4_000_000_000) == g.GEMM_OK
+    assert g.gemm_noalloc_set_option(g.GEMM_OPT_DEBUG_DROP_LOAD, 0) == g.GEMM_OK

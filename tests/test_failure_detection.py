@@ -25,7 +25,7 @@ CASES = [  # mode, layout, tensor-core mode, FP32 configuration (0 = chosen)
     ("f32", inp.B_ROW_MAJOR, None, 6),  # producer warpgroup with register reallocation
     ("f32", inp.B_COL_MAJOR, None, 6),  # the same, four producer warps turning B
     ("bf16", inp.B_ROW_MAJOR, 1, 0),
-    ("bf16", inp.B_ROW_MAJOR, 2, 0),
+    ("bf16", inp.B_ROW_MAJOR, 3, 0),
     ("bf16", inp.B_COL_MAJOR, 3, 0),
     ("tf32", inp.B_ROW_MAJOR, 3, 0),
 ]

@@ -405,29 +405,28 @@ CLUSTER_SHAPES = [(129, 257, 33), (257, 600, 64), (300, 520, 260), (385, 300, 10
                   (300, 448, 96)]  # whole 128-byte chunks of B, the last box half past N
 
 
-@pytest.mark.parametrize("cluster_mode", [2, 3])
 @pytest.mark.parametrize("mode", ["tf32", "bf16"])
 @pytest.mark.parametrize("layout", [ROW, COL])
 @pytest.mark.parametrize("shape", CLUSTER_SHAPES)
-def test_cluster_pairs_match_oracle_and_single_cta(g, oracle_mod, cluster_mode, mode, layout, shape):
-    """CTA pairs: mode 2 shares the B tile by TMA multicast, mode 3 runs the
-    pair MMA (tcgen05 cta_group::2, 256x256 per pair).  Odd tile-row counts
-    leave one CTA of the last pair entirely out of range.  Same parity, and
-    the same bits as the one-CTA kernel."""
+def test_cluster_pairs_match_oracle_and_single_cta(g, oracle_mod, mode, layout, shape):
+    """CTA pairs (mode 3) run the pair MMA (tcgen05 cta_group::2, 256x256
+    per pair).  Odd tile-row counts leave one CTA of the last pair entirely
+    out of range.  Same parity, and the same bits as the one-CTA kernel
+    (mode 1)."""
     from dense_gemm_sm100_gb300 import gemm
     M, N, K = shape
     A, B = inp.make_operands(M, N, K, layout_b=layout, dist="normal", seed=M + 3 * N + K, dtype=mode)
     g.set_option(gemm.GEMM_OPT_SPLIT_K, 1)  # these small shapes would otherwise be cut along K
     g.set_option(gemm.GEMM_OPT_TC_CLUSTER, 1)
     C1 = run_gpu(g, A, B, layout, mode).cpu()
-    assert "cluster2" not in g.last_path and "pair" not in g.last_path
-    g.set_option(gemm.GEMM_OPT_TC_CLUSTER, cluster_mode)
+    assert "pair" not in g.last_path
+    g.set_option(gemm.GEMM_OPT_TC_CLUSTER, 3)
     try:
         C2 = run_gpu(g, A, B, layout, mode).cpu()
-        assert ("cluster2" if cluster_mode == 2 else "pair256x256") in g.last_path
+        assert "pair256x256" in g.last_path
         # pair MMA with row-major B: one 3-D TMA box per stage when N is whole chunks
         chunk = 64 if mode == "bf16" else 32
-        b3d = cluster_mode == 3 and layout == ROW and M > 128 and N % chunk == 0
+        b3d = layout == ROW and M > 128 and N % chunk == 0
         assert ("+b3d" in g.last_path) == b3d, g.last_path
         # the one-CTA run above used the 3-D box under the same condition
         g.set_option(gemm.GEMM_OPT_TC_CLUSTER, 1)
@@ -437,8 +436,21 @@ def test_cluster_pairs_match_oracle_and_single_cta(g, oracle_mod, cluster_mode, 
         g.set_option(gemm.GEMM_OPT_TC_CLUSTER, 3)
         g.set_option(gemm.GEMM_OPT_SPLIT_K, 0)
     Cr, S = oracle_of(oracle_mod, A, B, layout)
-    assert_parity(C2, Cr, S, TOL[mode], f"cluster mode {cluster_mode} {mode} {shape}")
+    assert_parity(C2, Cr, S, TOL[mode], f"pair MMA {mode} {shape}")
     assert torch.equal(C1, C2)
+
+
+@pytest.mark.parametrize("value", [0, 2, 4, -1])
+def test_tc_cluster_option_accepts_only_one_cta_and_pair_modes(g, value):
+    """Only the one-CTA (1) and pair-MMA (3) tensor-core modes exist; any
+    other value is refused and leaves the handle's mode unchanged."""
+    from dense_gemm_sm100_gb300 import gemm
+    with pytest.raises(gemm.GemmError) as err:
+        g.set_option(gemm.GEMM_OPT_TC_CLUSTER, value)
+    assert err.value.code == gemm.GEMM_ERR_INVALID
+    A, B = inp.make_operands(300, 256, 64, layout_b=ROW, dist="normal", seed=5, dtype="bf16")
+    run_gpu(g, A, B, ROW, "bf16")
+    assert "pair256x256" in g.last_path
 
 
 @pytest.mark.parametrize("mode", ["tf32", "bf16"])

@@ -29,7 +29,7 @@ def cases():
         N = rng.choice([1, 3, 32, 64, 100, 128, 129, 256, 257, 448, 520, 640])
         K = rng.choice([1, 5, 16, 31, 32, 33, 64, 100, 256, 333, 512, 1000])
         simt_config = rng.choice([0, 0, 1, 6, 7]) if mode == "f32" else 0
-        tc_mode = rng.choice([1, 2, 3, 3]) if mode != "f32" else 3
+        tc_mode = rng.choice([1, 3, 3, 3]) if mode != "f32" else 3
         max_ctas = rng.choice([0, 0, 4, 8, 16])
         integer = rng.random() < 0.3
         elementwise = 1 if (mode == "f32" and layout == inp.B_ROW_MAJOR and rng.random() < 0.3) else 0
