@@ -106,6 +106,18 @@ __device__ __forceinline__ Unit unit_coords(int u, const SimtParams &p)
     return w;
 }
 
+// Number of K stages (k-tiles) of work unit u, as unit_coords would give
+// (kt_end - kt_begin) without the tile coordinates.
+__device__ __forceinline__ int unit_stages(int u, const SimtParams &p)
+{
+    const int k_tiles = (p.K + kSimtBK - 1) / kSimtBK;
+    if (u < p.full_units) return k_tiles;
+    const int split = (u - p.full_units) / p.tail_tiles;
+    const int k0 = split * p.k_per_split;
+    const int k1 = min(p.K, k0 + p.k_per_split);
+    return (k1 + kSimtBK - 1) / kSimtBK - k0 / kSimtBK;
+}
+
 // WM x WN consumer warps; a thread owns 8 rows x TN columns of C; STAGES ring
 // slots; GU k-groups (4 k each) per unrolled inner iteration (8 = a whole
 // stage); F2 = 1 issues the multiply-adds of row-major B as packed pairs
@@ -142,6 +154,11 @@ struct Simt {
     // PWG = 1: a producer warpgroup that gives up registers to the consumer
     // warpgroups (setmaxnreg), so a thread can hold a wider tile of C.
     static constexpr int PRODUCER_WARPS = PWG ? 4 : 1;
+    // Column-major B turned in shared memory: with a producer warpgroup, its
+    // first warp only issues the TMA copies and the other three turn the
+    // tiles (so neither role needs the other's registers); a single producer
+    // warp does both.
+    static constexpr int TURN_WARPS = PWG ? 3 : 1;
     static constexpr int THREADS = (CONSUMER_WARPS + PRODUCER_WARPS) * 32;
     static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8;  // what __launch_bounds__ allows
     // the corner turn (column-major B) and the element-wise copies need more
@@ -157,6 +174,10 @@ struct Simt {
     // 16 consumer warps leave 112 registers a thread: A fragments are then
     // loaded 2 k at a time (8-byte loads) instead of 4, to fit.
     static constexpr bool A_PAIRS = CONSUMER_WARPS >= 16;
+    // Explicitly double-buffered fragments with the column-pair-major,
+    // serpentine multiply-add order (packed FMAs on row-major staging, 8 x 8
+    // thread tiles, three consumer warps per scheduler).
+    static constexpr bool PINGPONG = F2 && LAYOUT_B != 1 && !A_PAIRS && GU == 8 && TN == 8 && CONSUMER_WARPS >= 12;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NBAR * STAGES * 8 + 16;
     static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
     static_assert(BM <= 256 && BN <= 256, "TMA box limit");
@@ -194,227 +215,322 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
             // arrival per producer thread when its copies have landed
             mbar_init(full_bar + 8 * s, LAYOUT_B == 3 ? S::PRODUCER_WARPS * 32 : 1);
             mbar_init(empty_bar + 8 * s, CONSUMER_WARPS);
-            if (LAYOUT_B == 2) mbar_init(ready_bar + 8 * s, S::PRODUCER_WARPS);  // every turning warp
+            if (LAYOUT_B == 2) mbar_init(ready_bar + 8 * s, S::TURN_WARPS);  // every turning warp
         }
         *abort_flag = 0;
         fence_barrier_init();
     }
     __syncthreads();
 
-    if (PWG) {
-        if (warp >= CONSUMER_WARPS) {
+    // Every producer role sits inside this one branch, after the register
+    // release: ptxas then budgets the consumer code below with the consumers'
+    // raised register count alone (producer code reachable after the branch
+    // would be compiled under the producers' small count, and spill).
+    if (warp >= CONSUMER_WARPS) {
+        if (PWG) {
             setmaxnreg_dec<S::PRODUCER_REGS>();
-            // one warp of the group issues the copies; with column-major B
-            // all four share the corner turn, with element-wise copies all
-            // four copy
+            // one warp of the group issues the copies; with column-major B the
+            // others turn the tiles, with element-wise copies all four copy
             if (warp != CONSUMER_WARPS && LAYOUT_B != 2 && LAYOUT_B != 3) return;
-        } else {
-            setmaxnreg_inc<S::CONSUMER_REGS>();
         }
-    }
 
-    if (LAYOUT_B == 3 && warp >= CONSUMER_WARPS) {
-        // ------------------------------------------- element-wise producer
-        // Thread pt of the PT producer threads copies elements pt, pt + PT,
-        // ... of the stage: consecutive threads take consecutive k of an A
-        // row and consecutive columns of a B row (coalesced reads; each warp
-        // writes one 128-byte swizzled row, 32 distinct banks).
-        constexpr int PT = S::PRODUCER_WARPS * 32;
-        const int pt = threadIdx.x - CONSUMER_WARPS * 32;
-        uint32_t it = 0;
-        bool ok = true;
-        for (int unit = blockIdx.x; ok && unit < num_units; unit += gridDim.x) {
-            const Unit w = unit_coords(unit, p);
-            for (int kt = w.kt_begin; kt < w.kt_end; ++kt, ++it) {
-                const uint32_t s = it % STAGES;
-                const uint32_t ph = (it / STAGES) & 1u;
-                bool got = true;
-                if (lane == 0)
-                    got = mbar_wait(empty_bar + 8 * s, ph ^ 1u, abort_flag, p.status, kWaitProducerEmpty,
-                                    p.timeout_ns);
-                if (__shfl_sync(0xffffffffu, got ? 1 : 0, 0) == 0) {
-                    ok = false;
-                    break;
+        if (LAYOUT_B == 3) {
+            // ------------------------------------------- element-wise producer
+            // Thread pt of the PT producer threads copies elements pt, pt + PT,
+            // ... of the stage: consecutive threads take consecutive k of an A
+            // row and consecutive columns of a B row (coalesced reads; each warp
+            // writes one 128-byte swizzled row, 32 distinct banks).
+            constexpr int PT = S::PRODUCER_WARPS * 32;
+            const int pt = threadIdx.x - CONSUMER_WARPS * 32;
+            uint32_t it = 0;
+            bool ok = true;
+            for (int unit = blockIdx.x; ok && unit < num_units; unit += gridDim.x) {
+                const Unit w = unit_coords(unit, p);
+                for (int kt = w.kt_begin; kt < w.kt_end; ++kt, ++it) {
+                    const uint32_t s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    bool got = true;
+                    if (lane == 0)
+                        got = mbar_wait(empty_bar + 8 * s, ph ^ 1u, abort_flag, p.status, kWaitProducerEmpty,
+                                        p.timeout_ns);
+                    if (__shfl_sync(0xffffffffu, got ? 1 : 0, 0) == 0) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t st = sbase + s * STAGE_BYTES;
+                    const int k0 = kt * BK;
+                    for (int e = pt; e < BM * BK; e += PT) {
+                        const int r = e / BK, kk = e - (e / BK) * BK;
+                        const long long m = (long long)w.mb * BM + r;
+                        const bool in = m < p.M && k0 + kk < p.K;
+                        const uint32_t dst = st + r * 128 + ((((kk >> 2) ^ (r & 7)) << 4) | ((kk & 3) << 2));
+                        cp_async_4(dst, in ? p.A + m * p.lda + k0 + kk : p.A, in ? 4u : 0u);
+                    }
+                    for (int e = pt; e < BK * BN; e += PT) {
+                        const int kk = e / BN, n = e - (e / BN) * BN;
+                        const long long col = (long long)w.nb * BN + n;
+                        const bool in = col < p.N && k0 + kk < p.K;
+                        const uint32_t dst = st + A_BYTES + (n >> 5) * 4096 + kk * 128 +
+                                             (((((n & 31) >> 2) ^ (kk & 7)) << 4) | ((n & 3) << 2));
+                        cp_async_4(dst, in ? p.B + (long long)(k0 + kk) * p.ldb + col : p.B, in ? 4u : 0u);
+                    }
+                    cp_async_mbar_arrive_noinc(full_bar + 8 * s);
                 }
-                const uint32_t st = sbase + s * STAGE_BYTES;
-                const int k0 = kt * BK;
-                for (int e = pt; e < BM * BK; e += PT) {
-                    const int r = e / BK, kk = e - (e / BK) * BK;
-                    const long long m = (long long)w.mb * BM + r;
-                    const bool in = m < p.M && k0 + kk < p.K;
-                    const uint32_t dst = st + r * 128 + ((((kk >> 2) ^ (r & 7)) << 4) | ((kk & 3) << 2));
-                    cp_async_4(dst, in ? p.A + m * p.lda + k0 + kk : p.A, in ? 4u : 0u);
-                }
-                for (int e = pt; e < BK * BN; e += PT) {
-                    const int kk = e / BN, n = e - (e / BN) * BN;
-                    const long long col = (long long)w.nb * BN + n;
-                    const bool in = col < p.N && k0 + kk < p.K;
-                    const uint32_t dst = st + A_BYTES + (n >> 5) * 4096 + kk * 128 +
-                                         (((((n & 31) >> 2) ^ (kk & 7)) << 4) | ((n & 3) << 2));
-                    cp_async_4(dst, in ? p.B + (long long)(k0 + kk) * p.ldb + col : p.B, in ? 4u : 0u);
-                }
-                cp_async_mbar_arrive_noinc(full_bar + 8 * s);
             }
+            cp_async_wait_all();  // no copy lands after the CTA has gone
+            return;
         }
-        cp_async_wait_all();  // no copy lands after the CTA has gone
-        return;
-    }
 
-    if (LAYOUT_B == 2 && warp >= CONSUMER_WARPS) {
-        // ------------------------------------------- producer + corner turn
-        // Lane 0 of the first producer warp keeps the ring STAGES-1 k-tiles
-        // ahead; the producer warps turn each landed K-major B tile (rows n,
-        // 128 bytes of k) into the row-major staging layout (4 boxes of 32
-        // k-rows x 32 columns, 128-byte swizzle) that the consumers read.
-        // Lane (g, t) = (lane/8, lane%8) moves 4x4 blocks of rows
-        // 4*(8g+t)..+3 and k-chunk t ^ r: inside each group of 8 lanes both
-        // the 16-byte reads and the 16-byte writes land on 8 distinct bank
-        // groups.  With P producer warps, warp w turns r = w*8/P .. +8/P-1;
-        // each arrives on the stage's ready barrier (count P) when done.
-        constexpr int R_PER = 8 / S::PRODUCER_WARPS;
-        const int pw = warp - CONSUMER_WARPS;
-        const bool issuer = pw == 0;
-        uint32_t issued = 0;
-        int iss_unit = blockIdx.x, iss_kt = 0, iss_kt_end = 0, iss_mb = 0, iss_nb = 0;
-        auto iss_load_unit = [&]() {
-            if (iss_unit < num_units) {
-                const Unit w = unit_coords(iss_unit, p);
-                iss_mb = w.mb;
-                iss_nb = w.nb;
-                iss_kt = w.kt_begin;
-                iss_kt_end = w.kt_end;
-            }
-        };
-        // lane 0: issue the next k-tile into its ring slot (bounded wait for the slot)
-        auto issue_next = [&]() -> bool {
-            const uint32_t slot = issued % STAGES;
-            const uint32_t ph = (issued / STAGES) & 1u;
-            if (!mbar_wait(empty_bar + 8 * slot, ph ^ 1u, abort_flag, p.status, kWaitProducerEmpty,
-                           p.timeout_ns))
-                return false;
-            const uint32_t fb = full_bar + 8 * slot;
-            const uint32_t st = sbase + slot * STAGE_BYTES;
-            mbar_arrive_expect_tx(fb, A_BYTES + S::LAND_BYTES);
-            if (!(p.debug_drop && blockIdx.x == 0 && issued == 0)) {
-                tma_load_2d(st, &tmA, fb, iss_kt * BK, iss_mb * BM);
-                tma_load_2d(st + LAND, &tmB, fb, iss_kt * BK, iss_nb * BN);
-            }
-            ++issued;
-            if (++iss_kt >= iss_kt_end) {
-                iss_unit += gridDim.x;
-                iss_load_unit();
-            }
-            return true;
-        };
-        bool ok = true;
-        if (issuer && lane == 0) {
+        if (LAYOUT_B == 2 && PWG && warp == CONSUMER_WARPS) {
+            // ------------------------------------- TMA issuer (column-major B)
+            // Lane 0 keeps every free ring slot loaded: A and the K-major B tile
+            // (into the landing zone).  A slot is free again once the consumers
+            // have released it, which they do only after the turn of its tile.
+            if (lane != 0) return;
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
-            iss_load_unit();
-            for (int i = 0; ok && i < STAGES - 1 && iss_unit < num_units; ++i) ok = issue_next();
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        const int tg = lane >> 3, tt = lane & 7;
-        const int nq = 8 * tg + tt;  // rows 4*nq .. 4*nq + 3 of the B tile
-        uint32_t it = 0;
-        for (int unit = blockIdx.x; ok && unit < num_units; unit += gridDim.x) {
-            const Unit w = unit_coords(unit, p);
-            for (int kt = w.kt_begin; ok && kt < w.kt_end; ++kt, ++it) {
-                const uint32_t s = it % STAGES;
-                const uint32_t ph = (it / STAGES) & 1u;
-                bool got = true;
-                if (lane == 0)
-                    got = mbar_wait(full_bar + 8 * s, ph, abort_flag, p.status, kWaitConsumerFull,
-                                    p.timeout_ns);
-                if (__shfl_sync(0xffffffffu, got ? 1 : 0, 0) == 0) {
-                    ok = false;
-                    break;
-                }
-                const uint8_t *land = smem + s * STAGE_BYTES + LAND;
-                uint8_t *brow = smem + s * STAGE_BYTES + A_BYTES + tg * 4096;
-#pragma unroll
-                for (int rr = 0; rr < R_PER; ++rr) {
-                    const int r = pw * R_PER + rr;
-                    const int c = tt ^ r;  // k chunk: k = 4c .. 4c + 3
-                    float4 v[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int n = 4 * nq + q;
-                        v[q] = *reinterpret_cast<const float4 *>(land + n * 128 + ((c ^ (n & 7)) << 4));
+            uint32_t it = 0;
+            bool ok = true;
+            for (int unit = blockIdx.x; ok && unit < num_units; unit += gridDim.x) {
+                const Unit w = unit_coords(unit, p);
+                for (int kt = w.kt_begin; kt < w.kt_end; ++kt, ++it) {
+                    const uint32_t s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (!mbar_wait(empty_bar + 8 * s, ph ^ 1u, abort_flag, p.status, kWaitProducerEmpty,
+                                   p.timeout_ns)) {
+                        ok = false;
+                        break;
                     }
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int k = 4 * c + e;
-                        const float4 o = e == 0 ? make_float4(v[0].x, v[1].x, v[2].x, v[3].x)
-                                       : e == 1 ? make_float4(v[0].y, v[1].y, v[2].y, v[3].y)
-                                       : e == 2 ? make_float4(v[0].z, v[1].z, v[2].z, v[3].z)
-                                                : make_float4(v[0].w, v[1].w, v[2].w, v[3].w);
-                        *reinterpret_cast<float4 *>(brow + k * 128 + ((tt ^ (k & 7)) << 4)) = o;
-                    }
+                    const uint32_t fb = full_bar + 8 * s;
+                    const uint32_t st = sbase + s * STAGE_BYTES;
+                    mbar_arrive_expect_tx(fb, A_BYTES + S::LAND_BYTES);
+                    if (p.debug_drop && blockIdx.x == 0 && it == 0) continue;  // bytes that never come
+                    tma_load_2d(st, &tmA, fb, kt * BK, w.mb * BM);
+                    tma_load_2d(st + LAND, &tmB, fb, kt * BK, w.nb * BN);
                 }
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(ready_bar + 8 * s);
-                    if (issuer && iss_unit < num_units) ok = issue_next();
+            }
+            if (!ok) {
+                // Leave no copy in flight: wait (bounded) for the stages issued last.
+                const uint32_t n = it < (uint32_t)STAGES ? it : (uint32_t)STAGES;
+                for (uint32_t i = it - n; i < it; ++i) {
+                    int dummy = 0;
+                    mbar_wait(full_bar + 8 * (i % STAGES), (i / STAGES) & 1u, &dummy, nullptr, kWaitDrain,
+                              p.timeout_ns);
                 }
-                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             }
+            return;
         }
-        if (!ok && issuer && lane == 0) {
-            // Leave no copy in flight: wait (bounded) for every stage issued
-            // but not yet turned.
-            for (uint32_t i = it; i < issued; ++i) {
-                int dummy = 0;
-                mbar_wait(full_bar + 8 * (i % STAGES), (i / STAGES) & 1u, &dummy, nullptr, kWaitDrain,
-                          p.timeout_ns);
-            }
-        }
-        return;
-    }
 
-    if (warp == CONSUMER_WARPS) {
-        // ------------------------------------------------------ producer
-        if (lane != 0) return;
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
-        uint32_t it = 0;
-        bool ok = true;
-        for (int unit = blockIdx.x; ok && unit < num_units; unit += gridDim.x) {
-            const Unit w = unit_coords(unit, p);
-            const int mb = w.mb, nb = w.nb;
-            for (int kt = w.kt_begin; kt < w.kt_end; ++kt, ++it) {
-                const uint32_t s = it % STAGES;
-                const uint32_t ph = (it / STAGES) & 1u;
-                if (!mbar_wait(empty_bar + 8 * s, ph ^ 1u, abort_flag, p.status,
-                               kWaitProducerEmpty, p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t fb = full_bar + 8 * s;
-                const uint32_t st = sbase + s * STAGE_BYTES;
-                mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                if (p.debug_drop && blockIdx.x == 0 && it == 0) continue;  // bytes that never come
-                tma_load_2d(st, &tmA, fb, kt * BK, mb * BM);
-                if (LAYOUT_B == 0) {
+        if (LAYOUT_B == 2 && PWG) {
+            // ------------------------------------------ corner turn (3 warps)
+            // Each landed K-major B tile (rows n, 128 bytes of k) is rewritten
+            // in the row-major staging layout (4 boxes of 32 k-rows x 32
+            // columns, 128-byte swizzle) that the consumers read.  Lane (g, t) =
+            // (lane/8, lane%8) moves 4x4 blocks of rows 4*(8g+t)..+3 and k-chunk
+            // t ^ r: inside each group of 8 lanes both the 16-byte reads and the
+            // 16-byte writes land on 8 distinct bank groups.  Turning warp q
+            // (0..2) moves k-chunks r = q, q + 3, q + 6 of every stage and then
+            // arrives on the stage's ready barrier (count 3).
+            const int q = warp - CONSUMER_WARPS - 1;
+            const int tg = lane >> 3, tt = lane & 7;
+            const int nq = 8 * tg + tt;  // rows 4*nq .. 4*nq + 3 of the B tile
+            uint32_t it = 0;
+            for (int unit = blockIdx.x; unit < num_units; unit += gridDim.x) {
+                const int stages = unit_stages(unit, p);
+                for (int j = 0; j < stages; ++j, ++it) {
+                    const uint32_t s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    bool got = true;
+                    if (lane == 0)
+                        got = mbar_wait(full_bar + 8 * s, ph, abort_flag, p.status, kWaitConsumerFull,
+                                        p.timeout_ns);
+                    if (__shfl_sync(0xffffffffu, got ? 1 : 0, 0) == 0) return;
+                    // 32-bit shared-memory addresses keep the turn within the
+                    // producers' register budget
+                    const uint32_t land = sbase + s * STAGE_BYTES + LAND + nq * 512;
+                    const uint32_t brow = sbase + s * STAGE_BYTES + A_BYTES + tg * 4096;
+#pragma unroll 1
+                    for (int r = q; r < 8; r += 3) {
+                        const int c = tt ^ r;  // k chunk: k = 4c .. 4c + 3
+                        // two rows at a time: rows 4*nq + 2h, +1 become the
+                        // 8-byte half h of the four k rows' 16-byte chunks
+#pragma unroll 1
+                        for (int h = 0; h < 2; ++h) {
+                            // row n = 4*nq + e, so n & 7 = 4*(tt & 1) + e
+                            const float4 v0 = lds_f4(land + (2 * h) * 128 + ((c ^ (4 * (tt & 1) + 2 * h)) << 4));
+                            const float4 v1 = lds_f4(land + (2 * h + 1) * 128 + ((c ^ (4 * (tt & 1) + 2 * h + 1)) << 4));
 #pragma unroll
-                    for (int j = 0; j < BN / 32; ++j)
-                        tma_load_2d(st + A_BYTES + j * 4096, &tmB, fb, nb * BN + 32 * j, kt * BK);
-                } else {
-                    tma_load_2d(st + A_BYTES, &tmB, fb, kt * BK, nb * BN);
+                            for (int e = 0; e < 4; ++e) {
+                                const int k = 4 * c + e;
+                                const float2 o = e == 0 ? make_float2(v0.x, v1.x)
+                                               : e == 1 ? make_float2(v0.y, v1.y)
+                                               : e == 2 ? make_float2(v0.z, v1.z)
+                                                        : make_float2(v0.w, v1.w);
+                                sts_f2(brow + k * 128 + ((tt ^ (k & 7)) << 4) + 8 * h, o);
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(ready_bar + 8 * s);
                 }
             }
+            return;
         }
-        if (!ok) {
-            // Leave no copy in flight: wait (bounded) for the stages issued last.
-            const uint32_t n = it < (uint32_t)STAGES ? it : (uint32_t)STAGES;
-            for (uint32_t i = it - n; i < it; ++i) {
-                int dummy = 0;
-                mbar_wait(full_bar + 8 * (i % STAGES), (i / STAGES) & 1u, &dummy, nullptr,
-                          kWaitDrain, p.timeout_ns);
+
+        if (LAYOUT_B == 2) {
+            // -------------------- single producer warp: issue + corner turn
+            // Lane 0 keeps the ring STAGES-1 k-tiles ahead; the warp turns each
+            // landed K-major B tile into the row-major staging layout with the
+            // lane mapping of the three-warp form above (all 8 k-chunks), then
+            // arrives on the stage's ready barrier (count 1).
+            constexpr int R_PER = 8 / S::PRODUCER_WARPS;
+            const int pw = warp - CONSUMER_WARPS;
+            const bool issuer = pw == 0;
+            uint32_t issued = 0;
+            int iss_unit = blockIdx.x, iss_kt = 0, iss_kt_end = 0, iss_mb = 0, iss_nb = 0;
+            auto iss_load_unit = [&]() {
+                if (iss_unit < num_units) {
+                    const Unit w = unit_coords(iss_unit, p);
+                    iss_mb = w.mb;
+                    iss_nb = w.nb;
+                    iss_kt = w.kt_begin;
+                    iss_kt_end = w.kt_end;
+                }
+            };
+            // lane 0: issue the next k-tile into its ring slot (bounded wait for the slot)
+            auto issue_next = [&]() -> bool {
+                const uint32_t slot = issued % STAGES;
+                const uint32_t ph = (issued / STAGES) & 1u;
+                if (!mbar_wait(empty_bar + 8 * slot, ph ^ 1u, abort_flag, p.status, kWaitProducerEmpty,
+                               p.timeout_ns))
+                    return false;
+                const uint32_t fb = full_bar + 8 * slot;
+                const uint32_t st = sbase + slot * STAGE_BYTES;
+                mbar_arrive_expect_tx(fb, A_BYTES + S::LAND_BYTES);
+                if (!(p.debug_drop && blockIdx.x == 0 && issued == 0)) {
+                    tma_load_2d(st, &tmA, fb, iss_kt * BK, iss_mb * BM);
+                    tma_load_2d(st + LAND, &tmB, fb, iss_kt * BK, iss_nb * BN);
+                }
+                ++issued;
+                if (++iss_kt >= iss_kt_end) {
+                    iss_unit += gridDim.x;
+                    iss_load_unit();
+                }
+                return true;
+            };
+            bool ok = true;
+            if (issuer && lane == 0) {
+                tma_prefetch_desc(&tmA);
+                tma_prefetch_desc(&tmB);
+                iss_load_unit();
+                for (int i = 0; ok && i < STAGES - 1 && iss_unit < num_units; ++i) ok = issue_next();
             }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            const int tg = lane >> 3, tt = lane & 7;
+            const int nq = 8 * tg + tt;  // rows 4*nq .. 4*nq + 3 of the B tile
+            uint32_t it = 0;
+            for (int unit = blockIdx.x; ok && unit < num_units; unit += gridDim.x) {
+                const Unit w = unit_coords(unit, p);
+                for (int kt = w.kt_begin; ok && kt < w.kt_end; ++kt, ++it) {
+                    const uint32_t s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    bool got = true;
+                    if (lane == 0)
+                        got = mbar_wait(full_bar + 8 * s, ph, abort_flag, p.status, kWaitConsumerFull,
+                                        p.timeout_ns);
+                    if (__shfl_sync(0xffffffffu, got ? 1 : 0, 0) == 0) {
+                        ok = false;
+                        break;
+                    }
+                    const uint8_t *land = smem + s * STAGE_BYTES + LAND;
+                    uint8_t *brow = smem + s * STAGE_BYTES + A_BYTES + tg * 4096;
+#pragma unroll
+                    for (int rr = 0; rr < R_PER; ++rr) {
+                        const int r = pw * R_PER + rr;
+                        const int c = tt ^ r;  // k chunk: k = 4c .. 4c + 3
+                        float4 v[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int n = 4 * nq + q;
+                            v[q] = *reinterpret_cast<const float4 *>(land + n * 128 + ((c ^ (n & 7)) << 4));
+                        }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int k = 4 * c + e;
+                            const float4 o = e == 0 ? make_float4(v[0].x, v[1].x, v[2].x, v[3].x)
+                                           : e == 1 ? make_float4(v[0].y, v[1].y, v[2].y, v[3].y)
+                                           : e == 2 ? make_float4(v[0].z, v[1].z, v[2].z, v[3].z)
+                                                    : make_float4(v[0].w, v[1].w, v[2].w, v[3].w);
+                            *reinterpret_cast<float4 *>(brow + k * 128 + ((tt ^ (k & 7)) << 4)) = o;
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(ready_bar + 8 * s);
+                        if (issuer && iss_unit < num_units) ok = issue_next();
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                }
+            }
+            if (!ok && issuer && lane == 0) {
+                // Leave no copy in flight: wait (bounded) for every stage issued
+                // but not yet turned.
+                for (uint32_t i = it; i < issued; ++i) {
+                    int dummy = 0;
+                    mbar_wait(full_bar + 8 * (i % STAGES), (i / STAGES) & 1u, &dummy, nullptr, kWaitDrain,
+                              p.timeout_ns);
+                }
+            }
+            return;
         }
-        return;
-    }
+
+        {
+            // ------------------------------------------------------ producer
+            if (lane != 0) return;
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int unit = blockIdx.x; ok && unit < num_units; unit += gridDim.x) {
+                const Unit w = unit_coords(unit, p);
+                const int mb = w.mb, nb = w.nb;
+                for (int kt = w.kt_begin; kt < w.kt_end; ++kt, ++it) {
+                    const uint32_t s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (!mbar_wait(empty_bar + 8 * s, ph ^ 1u, abort_flag, p.status,
+                                   kWaitProducerEmpty, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full_bar + 8 * s;
+                    const uint32_t st = sbase + s * STAGE_BYTES;
+                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    if (p.debug_drop && blockIdx.x == 0 && it == 0) continue;  // bytes that never come
+                    tma_load_2d(st, &tmA, fb, kt * BK, mb * BM);
+                    if (LAYOUT_B == 0) {
+#pragma unroll
+                        for (int j = 0; j < BN / 32; ++j)
+                            tma_load_2d(st + A_BYTES + j * 4096, &tmB, fb, nb * BN + 32 * j, kt * BK);
+                    } else {
+                        tma_load_2d(st + A_BYTES, &tmB, fb, kt * BK, nb * BN);
+                    }
+                }
+            }
+            if (!ok) {
+                // Leave no copy in flight: wait (bounded) for the stages issued last.
+                const uint32_t n = it < (uint32_t)STAGES ? it : (uint32_t)STAGES;
+                for (uint32_t i = it - n; i < it; ++i) {
+                    int dummy = 0;
+                    mbar_wait(full_bar + 8 * (i % STAGES), (i / STAGES) & 1u, &dummy, nullptr,
+                              kWaitDrain, p.timeout_ns);
+                }
+            }
+            return;
+        }
+
+    }  // producer roles
+
+    if (PWG) setmaxnreg_inc<S::CONSUMER_REGS>();
 
     // ---------------------------------------------------------- consumers
     const int wm = warp % WM;
@@ -454,6 +570,61 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
                                             kWaitConsumerFull, p.timeout_ns))
                 return;
             const uint8_t *st = smem + s * STAGE_BYTES;
+            if (S::PINGPONG) {
+                // Fragment double buffering ("GEMM 性能优化", 台阶 6, p-Loop
+                // level): the A fragments of k group g+1 and the B fragment of
+                // row k+1 are loaded while row k is multiplied.  The packed
+                // multiply-adds run column pair by column pair (each B pair
+                // serves 8 consecutive instructions) with the row order
+                // reversed on every other pair, so the A value at the turn is
+                // also reused: 67.2 -> 70.6 TFLOP/s at whole waves on GB300,
+                // same bits (each accumulator still sums k in order).
+                constexpr int NC = TN / 4;  // 16-byte B chunks per k row
+                float4 a[2][8];
+                float4 b[2][NC];
+                {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        a[0][i] = *reinterpret_cast<const float4 *>(st + a_base + (xa << 4) + i * 1024);
+                    const uint8_t *bp = st + b_base + (lc << 4);
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) b[0][c] = *reinterpret_cast<const float4 *>(bp + c * 4096);
+                }
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const int k = 4 * g + kk;
+                        if (k + 1 < BK) {
+                            const int kn = k + 1;
+                            const uint8_t *bp = st + b_base + kn * 128 + ((lc ^ (kn & 7)) << 4);
+#pragma unroll
+                            for (int c = 0; c < NC; ++c) b[kn & 1][c] = *reinterpret_cast<const float4 *>(bp + c * 4096);
+                        }
+                        if (kk == 0 && g + 1 < 8) {
+                            const uint8_t *ap = st + a_base + (((g + 1) ^ xa) << 4);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) a[(g + 1) & 1][i] = *reinterpret_cast<const float4 *>(ap + i * 1024);
+                        }
+                        float2 b2[TN / 2];
+#pragma unroll
+                        for (int c = 0; c < NC; ++c) {
+                            const float4 b4 = b[k & 1][c];
+                            b2[2 * c] = make_float2(b4.x, b4.y);
+                            b2[2 * c + 1] = make_float2(b4.z, b4.w);
+                        }
+#pragma unroll
+                        for (int jp = 0; jp < TN / 2; ++jp)
+#pragma unroll
+                            for (int r = 0; r < 8; ++r) {
+                                const int i = (jp & 1) ? 7 - r : r;
+                                const float4 ai = a[g & 1][i];
+                                const float av = kk == 0 ? ai.x : kk == 1 ? ai.y : kk == 2 ? ai.z : ai.w;
+                                acc2[i][jp] = __ffma2_rn(make_float2(av, av), b2[jp], acc2[i][jp]);
+                            }
+                    }
+                }
+            } else
 #pragma unroll 1
             for (int g0 = 0; g0 < 8; g0 += GU) {
 #pragma unroll
