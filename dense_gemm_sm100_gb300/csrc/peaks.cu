@@ -6,7 +6,11 @@
 //  * FP32 fused multiply-adds on the CUDA cores, scalar (fma.rn.f32) or packed
 //    in pairs (fma.rn.f32x2), as the SIMT GEMM issues them.  Every thread runs
 //    independent chains x <- x * a + b that stay near 1 (no overflow, no
-//    subnormals); 32 warps per SM hide the FMA latency.
+//    subnormals); 32 warps per SM hide the FMA latency.  Each chain starts
+//    from a value that depends on the thread, so the compiler can neither
+//    merge chains nor evaluate one at compile time: a chain started exactly
+//    at the fixed point x = 1 (1 * 0.999 + 0.001 rounds to 1 in FP32) was
+//    once folded away, and the FLOP count then overstated the work by 16/15.
 //  * tcgen05 MMAs from shared memory into tensor memory, BF16 or TF32 inputs
 //    with FP32 accumulation, M = 128, N = 256 (one CTA per SM), as the
 //    tensor-core GEMM issues them but with operands that stay in shared
@@ -34,7 +38,8 @@ __global__ void __launch_bounds__(kFmaThreads) fma_peak_kernel(int packed, long 
     float2 acc[kFmaChains];
 #pragma unroll
     for (int c = 0; c < kFmaChains; ++c)
-        acc[c] = make_float2(1.0f + 1e-3f * c, 1.0f - 1e-3f * (threadIdx.x & 7));
+        acc[c] = make_float2(0.5f + 0.03125f * c + 0.0009765625f * (threadIdx.x & 31),
+                             0.25f + 0.03125f * c + 0.0009765625f * (threadIdx.x & 31));
     const float2 a = make_float2(0.999f, 0.999f), b = make_float2(0.001f, 0.001f);
     if (packed) {
         for (long long i = 0; i < iters; i += kFmaUnroll)
