@@ -1,9 +1,12 @@
 """Benchmark of the GB300 GEMM library: TFLOPS = 2MNK/t and roofline fraction.
 
 Default workload: FP32 SIMT GEMM, M = N = K = 8192, A, B, C row-major, values
-U[-1, 1) from seed 3 (the SIMT headline case).  The same run also measures the
-tensor-core headline case (FFN-shaped M=8192, N=14336, K=4096, N(0, 0.02) from
-seed 4, BF16 and TF32 inputs, FP32 C) and reports it under "modes".
+U[-1, 1) from seed 3 (the SIMT headline case).  The same run also measures,
+under "modes", every other specified workload: the tensor-core headline case
+(FFN-shaped M=8192, N=14336, K=4096, N(0, 0.02) from seed 4, BF16 and TF32
+inputs, FP32 C), the FP32 cases 128^3, 1024^3 with column-major B and
+4095x3073x2047, and the extra FP32-accurate tensor-core mode; each mode
+records the steps and warm-up steps it ran.
 
 One step = one gemm_run of the whole workload through the C ABI with inputs
 resident in HBM.  Inputs are larger than L2, so no flush is needed.
@@ -34,6 +37,13 @@ METRIC = "GEMM TFLOPS (2MNK/t) and % of GB300 FP32-SIMT / tensor-core roofline"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "fp32_8192_row"
 TC_WORKLOADS = ["ffn_bf16_8192x14336x4096", "ffn_tf32_8192x14336x4096", "fp32x3_8192_row"]
+# The other specified FP32 workloads, measured under "modes" too.
+SIMT_WORKLOADS = ["fp32_128_row", "fp32_1024_colB", "fp32_4095x3073x2047_row"]
+# Modes whose step is short run at least this many timed steps (recorded in
+# the mode's "steps"): the tensor-core modes reach their steady power state,
+# and the microsecond-scale FP32 cases get a stable mean.
+MIN_MODE_STEPS = {"ffn_bf16_8192x14336x4096": 200, "ffn_tf32_8192x14336x4096": 200,
+                  "fp32x3_8192_row": 100, "fp32_128_row": 200, "fp32_1024_colB": 200}
 
 # Fallback peaks (one earlier GB300 measurement) if MEASURED_PEAKS.json is absent.
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
@@ -43,15 +53,10 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 NOMINAL_PF = {"bf16": 2.25, "tf32": 1.1, "f32x3": 1.1 / 3}  # f32x3: three TF32 products per FP32 one
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
-# ncu capture of the kernel as it is now; None until captured for this version.
+# ncu capture of the kernel as it is now; absent (reported as null) until
+# captured for this version of the kernel.
 # Key: workload name -> (bytes per launch, summary file under profiles/).
-NCU_TRAFFIC: dict[str, tuple[float, str]] = {
-    "fp32_8192_row": (2714.6e6 + 260.8e6, "profiles/dram_traffic_full_size.md"),
-    "ffn_bf16_8192x14336x4096": (483.6e6 + 433.7e6, "profiles/dram_traffic_full_size.md"),
-    "ffn_tf32_8192x14336x4096": (1817.0e6 + 446.0e6, "profiles/dram_traffic_full_size.md"),
-    # the dominant kernel of the mode: the TF32 product over 3K
-    "fp32x3_8192_row": (8557.0e6 + 259.2e6, "profiles/dram_traffic_full_size.md"),
-}
+NCU_TRAFFIC: dict[str, tuple[float, str]] = {}
 
 DESCRIPTIONS = {
     "fp32_8192_row": "FP32 SIMT GEMM M=N=K=8192, A/B/C row-major, U[-1,1) seed 3",
@@ -93,14 +98,28 @@ def roofline_entry(bound, achieved, peak, unit, traffic, note):
             "traffic": traffic, "peak_source": note}
 
 
-def measure_peaks():
+def measure_peaks(dev_index=0, max_mhz=None):
     """The compute roofs measured on this GPU by the library's own
-    microbenchmarks (include/gemm_peaks.h), each launch ~20-50 ms, best of 3."""
+    microbenchmarks (include/gemm_peaks.h), each launch ~20-50 ms, best of 3,
+    with the SM clock sampled while they ran: the FP32 readings are also
+    given scaled to the maximum clock (rate x max MHz / median MHz), which
+    can never exceed SMs x 128 x 2 x the maximum clock."""
     from dense_gemm_sm100_gb300 import gemm
     out = {}
+    sampler = ClockSampler(dev_index)
+    sampler.start()
+    t0 = time.time()
     for kind, iters in (("ffma", 320000), ("ffma2", 320000), ("mma_bf16", 64000), ("mma_tf32", 64000)):
         r = gemm.measure_peak(kind, iters)
         out[f"{kind}_tflops"] = round(r["tflops"], 2)
+        if kind == "ffma2":
+            t_fma = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t0, t_fma)
+    if clocks and clocks.get("sm_mhz") and max_mhz:
+        out["fma_clocks"] = clocks
+        for kind in ("ffma", "ffma2"):
+            out[f"{kind}_tflops_at_max_clock"] = round(out[f"{kind}_tflops"] * max_mhz / clocks["sm_mhz"], 2)
     out["what"] = ("FP32 multiply-adds on the CUDA cores, scalar and packed pairs (32 warps/SM of "
                    "independent chains); tcgen05 MMA 128x256 from shared memory into tensor memory, "
                    "one CTA per SM, no copies")
@@ -286,15 +305,15 @@ def bench_workload(g, name, steps, warmup, dist_ctx, peaks, peak_note, with_e2e,
         def run_host():
             g.run_host(Ah, Bh, Ch, w.layout_b, w.dtype, stream)
 
-        e2e_steps = max(2, min(steps, 10))
-        e2e_ms, _, _ = time_device(run_host, stream, e2e_steps, 2)
+        e2e_ms, _, _ = time_device(run_host, stream, steps, warmup)
         g.sync_status(stream)
-        e2e_ms_all = all_gather_max(dist_ctx, e2e_ms / e2e_steps)
+        e2e_ms_all = all_gather_max(dist_ctx, e2e_ms / steps)
         _, e2e_value = aggregate(e2e_ms_all, w.flops)
         res["e2e"] = {"value": e2e_value, "unit": UNIT,
                       "h2d_bytes_per_step": A.numel() * A.element_size() + B.numel() * B.element_size(),
                       "d2h_bytes_per_step": w.M * w.N * 4,
-                      "ms_per_step": max(e2e_ms_all)}
+                      "ms_per_step": max(e2e_ms_all), "steps": steps, "warmup": warmup,
+                      "path": g.last_path}
     del A_d, B_d, C_d
     torch.cuda.empty_cache()
     return res
@@ -710,20 +729,28 @@ def main(argv=None):
             r["frac_at_observed_clock"] = round(r["achieved"] / (r["peak"] * f), 4) if f > 0 else None
     measured = None
     if not args.no_peaks:
-        measured = measure_peaks()
+        measured = measure_peaks(dev_index, peaks["sm_max_mhz"])
         if measured:
-            add_microbench(main_res["roofline"], measured.get("ffma2_tflops"))
+            # the higher of the scalar and packed FMA readings is the FP32 roof
+            add_microbench(main_res["roofline"],
+                           max(measured.get("ffma_tflops") or 0.0, measured.get("ffma2_tflops") or 0.0))
     modes = []
     if not args.no_modes:
-        for name in TC_WORKLOADS:
+        for name in TC_WORKLOADS + SIMT_WORKLOADS:
             msampler = ClockSampler(dev_index) if rank0 else None
             if msampler:
                 msampler.start()
-            r = bench_workload(g, name, max(args.steps, 200), args.warmup, ctx, peaks, peak_note,
+            mode_steps = max(args.steps, MIN_MODE_STEPS.get(name, 0))
+            r = bench_workload(g, name, mode_steps, args.warmup, ctx, peaks, peak_note,
                                with_e2e=False, side_cublas=not args.no_side_reference)
             m = {k: r[k] for k in ("workload", "description", "dtype", "value",
-                                   "ms_per_step", "kernel_ms", "path", "roofline")}
-            if measured:
+                                   "ms_per_step", "kernel_ms", "kernel_ms_median", "path", "roofline")}
+            m["steps"], m["warmup"] = mode_steps, args.warmup
+            m["l2"] = l2_note(r)
+            if r["dtype"] == "f32" and measured:
+                add_microbench(m["roofline"], max(measured.get("ffma_tflops") or 0.0,
+                                                  measured.get("ffma2_tflops") or 0.0))
+            elif measured:
                 mb = measured.get(f"mma_{r['dtype']}_tflops")
                 if r["dtype"] == "f32x3" and measured.get("mma_tf32_tflops"):
                     mb = measured["mma_tf32_tflops"] / 3
@@ -741,6 +768,7 @@ def main(argv=None):
             modes.append(m)
     e2e = None
     if not args.no_e2e:
+        # the host-buffer step moves 768 MiB over the host link: 10 steps
         r = bench_workload(g, args.workload, min(args.steps, 10), args.warmup, ctx, peaks,
                            peak_note, with_e2e=True)
         e2e = r["e2e"]

@@ -83,18 +83,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete is suspended
+// until it completes or up to `kWaitSuspendNs` have passed, instead of the
+// hardware's own short limit: a waiting warp then stops taking issue slots
+// from the warps that compute (column-major FP32: 64.7 -> 67.1 TFLOP/s).
+constexpr uint32_t kWaitSuspendNs = 20000;
+
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(kWaitSuspendNs)
+        : "memory");
+    return done != 0;
+}
+
 // Wait until the barrier phase with the given parity has completed, for at
-// most `timeout_ns`.  Gives up early when another thread of the CTA has set
-// `*abort`.  On expiry it sets `*abort`, records `site` in the status word and
-// returns false; the caller then leaves its loop.  The first try costs one
-// try_wait; the clock is only read on the slow path.
+// most `timeout_ns` (checked every 16 suspended tries, so to within about
+// 16 x kWaitSuspendNs).  Gives up early when another thread of the CTA has
+// set `*abort`.  On expiry it sets `*abort`, records `site` in the status
+// word and returns false; the caller then leaves its loop.  The first try
+// costs one try_wait; the clock is only read on the slow path.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
                                           int *status, int site, uint64_t timeout_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t spin = 1;; ++spin) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_suspend(bar, parity)) return true;
         if ((spin & 15u) == 0) {
             if (*abort) return false;
             if (global_timer_ns() - t0 > timeout_ns) {

@@ -176,8 +176,8 @@ struct Simt {
     static constexpr bool A_PAIRS = CONSUMER_WARPS >= 16;
     // Explicitly double-buffered fragments with the column-pair-major,
     // serpentine multiply-add order (packed FMAs on row-major staging, 8 x 8
-    // thread tiles, three consumer warps per scheduler).
-    static constexpr bool PINGPONG = F2 && LAYOUT_B != 1 && !A_PAIRS && GU == 8 && TN == 8 && CONSUMER_WARPS >= 12;
+    // thread tiles, 8 or 12 consumer warps).
+    static constexpr bool PINGPONG = F2 && LAYOUT_B != 1 && !A_PAIRS && GU == 8 && TN == 8 && CONSUMER_WARPS >= 8;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NBAR * STAGES * 8 + 16;
     static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
     static_assert(BM <= 256 && BN <= 256, "TMA box limit");
@@ -353,9 +353,13 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
                     for (int r = q; r < 8; r += 3) {
                         const int c = tt ^ r;  // k chunk: k = 4c .. 4c + 3
                         // two rows at a time: rows 4*nq + 2h, +1 become the
-                        // 8-byte half h of the four k rows' 16-byte chunks
+                        // 8-byte half h of the four k rows' 16-byte chunks.
+                        // The lane groups of odd tg take the halves in the
+                        // other order, so each 8-byte store instruction puts
+                        // two groups on different banks (2 wavefronts, not 4).
 #pragma unroll 1
-                        for (int h = 0; h < 2; ++h) {
+                        for (int hs = 0; hs < 2; ++hs) {
+                            const int h = hs ^ (tg & 1);
                             // row n = 4*nq + e, so n & 7 = 4*(tt & 1) + e
                             const float4 v0 = lds_f4(land + (2 * h) * 128 + ((c ^ (4 * (tt & 1) + 2 * h)) << 4));
                             const float4 v1 = lds_f4(land + (2 * h + 1) * 128 + ((c ^ (4 * (tt & 1) + 2 * h + 1)) << 4));
@@ -873,28 +877,25 @@ void launch_cfg(int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB, co
      prepare_cfg<WM, WN, TN, ST, GU, F2, PWG>, launch_cfg<WM, WN, TN, ST, GU, F2, PWG>}
 
 // Config table; GEMM_OPT_SIMT_CONFIG selects entry (value - 1).  Rates are
-// TFLOP/s measured on GB300 at sizes that fill whole waves (M = 7296 or
-// 14592, N = 8192); simt_pick_config weighs them against each shape's
-// waves.  The scalar-FMA, 64x128 and 64x64 tiles (56.4, 59.2 and 31.5 at
-// 8192^3), 128x256 with register reallocation (8x16 per thread, 64.0) and
-// 16 consumer warps of 8x8 with A loaded in pairs (256x128, 112 registers,
-// spills: 59.3) never win; they stay selectable.  More consumer warps per
-// scheduler hide the multiply-add latency better: 12 (3 per scheduler,
-// 192x128) against 8, 67.4 against 64.4 (column-major B, its corner turn
-// shared by the four producer warps, 62.3 against 60.0), and for 128x128
-// tiles 16 warps of 8x4 (4 per scheduler, register reallocation) against 8
-// of 8x8, 66.4 against 64.4 with row-major B (2-3 % on every shape
-// measured, 4095x3073x2047 included) but 59.2 against 60.0 column-major.
-// With scalar FMAs instead of packed pairs the 192x128 tile is issue-bound
-// (57.7).
+// TFLOP/s measured on GB300 at sizes that fill whole waves (M = 7296,
+// N = K = 8192); simt_pick_config weighs them against each shape's waves.
+// With the double-buffered, column-pair-major inner loop (8 x 8 thread
+// tiles): 192x128 with 12 consumer warps 70.3 row-major / 67.1 column-major
+// B, 128x128 with 8 consumer warps 69.0 / 63.5.  16 consumer warps of 8 x 4
+// (128x128w16, A loaded in pairs, row-pair-major order) 66.6 row-major.  The
+// scalar-FMA, 64x128 and 64x64 tiles (56.4, 59.2 and 31.5 at 8192^3 before
+// the new inner loop), 128x256 with register reallocation (8x16 per thread,
+// 64.0) and 16 consumer warps of 8x8 with A loaded in pairs (256x128, 112
+// registers, spills: 59.3) never win; they stay selectable.  With scalar
+// FMAs instead of packed pairs the 192x128 tile is issue-bound (57.7).
 ConfigEntry g_configs[] = {
-    DG_SIMT_CFG(4, 2, 8, 6, 8, 1, 0, 64.9f, 60.0f, "128x128"),
+    DG_SIMT_CFG(4, 2, 8, 6, 8, 1, 0, 69.0f, 63.5f, "128x128"),
     DG_SIMT_CFG(4, 2, 8, 6, 8, 0, 0, 0.0f, 0.0f, "128x128s"),
     DG_SIMT_CFG(2, 2, 8, 4, 8, 1, 0, 0.0f, 0.0f, "64x128"),
     DG_SIMT_CFG(2, 1, 8, 4, 8, 1, 0, 0.0f, 0.0f, "64x64"),
     DG_SIMT_CFG(4, 2, 16, 4, 8, 1, 1, 0.0f, 0.0f, "128x256r"),
-    DG_SIMT_CFG(6, 2, 8, 4, 8, 1, 1, 67.3f, 62.3f, "192x128r"),
-    DG_SIMT_CFG(4, 4, 4, 6, 8, 1, 1, 66.4f, 0.0f, "128x128w16"),
+    DG_SIMT_CFG(6, 2, 8, 4, 8, 1, 1, 70.3f, 67.1f, "192x128r"),
+    DG_SIMT_CFG(4, 4, 4, 6, 8, 1, 1, 66.6f, 0.0f, "128x128w16"),
     DG_SIMT_CFG(8, 2, 8, 4, 8, 1, 1, 0.0f, 0.0f, "256x128r"),
 };
 constexpr int kNumConfigs = sizeof(g_configs) / sizeof(g_configs[0]);

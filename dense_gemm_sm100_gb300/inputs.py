@@ -73,6 +73,12 @@ PROFILE_WORKLOADS = {
     # 19 x 32 tiles of 192 x 128 = 4 whole waves on 152 SMs; A, B, C 184 MiB
     "fp32_3648x4096x4096_row": Workload("fp32_3648x4096x4096_row", 3648, 4096, 4096, B_ROW_MAJOR,
                                         "uniform", 3),
+    # the same with B column-major (the corner-turning kernel)
+    "fp32_3648x4096x4096_colB": Workload("fp32_3648x4096x4096_colB", 3648, 4096, 4096, B_COL_MAJOR,
+                                         "uniform", 3),
+    # 19 x 32 tiles of 128 x 128 = 4 whole waves on 152 SMs; A, B, C 140 MiB
+    "fp32_2432x4096x4096_row": Workload("fp32_2432x4096x4096_row", 2432, 4096, 4096, B_ROW_MAJOR,
+                                        "uniform", 3),
     "ffn_bf16_4096x7168x4096": Workload("ffn_bf16_4096x7168x4096", 4096, 7168, 4096,
                                         B_ROW_MAJOR, "normal", 4, 0.02, BF16),
     "ffn_tf32_4096x7168x4096": Workload("ffn_tf32_4096x7168x4096", 4096, 7168, 4096,

@@ -116,3 +116,16 @@ def test_tensor_modes_are_described_and_peaked():
     w = inputs.ALL_WORKLOADS["fp32x3_8192_row"]
     ref = inputs.WORKLOADS["fp32_8192_row"]
     assert (w.M, w.N, w.K, w.layout_b, w.dist, w.seed) == (ref.M, ref.N, ref.K, ref.layout_b, ref.dist, ref.seed)
+
+
+def test_every_specified_workload_is_a_bench_mode():
+    """The default bench line covers every specified workload: the headline
+    FP32 8192^3 case as `value`, and the other four (128^3, 1024^3 with
+    column-major B, 4095x3073x2047, and the FFN shape in BF16 and TF32) under
+    `modes`, each described; a mode's minimum step count is what it records."""
+    from dense_gemm_sm100_gb300 import inputs
+    covered = {bench.DEFAULT_WORKLOAD, *bench.TC_WORKLOADS, *bench.SIMT_WORKLOADS}
+    assert set(inputs.WORKLOADS) <= covered
+    for name in bench.SIMT_WORKLOADS:
+        assert name in bench.DESCRIPTIONS and inputs.ALL_WORKLOADS[name].dtype == "f32"
+    assert all(v >= 1 for v in bench.MIN_MODE_STEPS.values())
