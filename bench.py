@@ -56,7 +56,14 @@ NOMINAL_PF = {"bf16": 2.25, "tf32": 1.1, "f32x3": 1.1 / 3}  # f32x3: three TF32 
 # ncu capture of the kernel as it is now; absent (reported as null) until
 # captured for this version of the kernel.
 # Key: workload name -> (bytes per launch, summary file under profiles/).
-NCU_TRAFFIC: dict[str, tuple[float, str]] = {}
+NCU_TRAFFIC: dict[str, tuple[float, str]] = {
+    "fp32_8192_row": (2712.5e6 + 258.1e6, "profiles/dram_traffic_per_kernel.md"),
+    "fp32_4095x3073x2047_row": (60.7e6 + 19.6e6, "profiles/dram_traffic_per_kernel.md"),
+    "ffn_bf16_8192x14336x4096": (498.0e6 + 439.8e6, "profiles/dram_traffic_per_kernel.md"),
+    "ffn_tf32_8192x14336x4096": (2370.8e6 + 455.2e6, "profiles/dram_traffic_per_kernel.md"),
+    # the dominant kernel of the mode: the TF32 product over 3K
+    "fp32x3_8192_row": (16186.3e6 + 265.3e6, "profiles/dram_traffic_per_kernel.md"),
+}
 
 DESCRIPTIONS = {
     "fp32_8192_row": "FP32 SIMT GEMM M=N=K=8192, A/B/C row-major, U[-1,1) seed 3",
@@ -666,6 +673,8 @@ def main(argv=None):
                     help="skip the FMA and tensor-core peak microbenchmarks")
     ap.add_argument("--no-side-reference", action="store_true",
                     help="skip the labelled cuBLAS side reference")
+    ap.add_argument("--peaks-only", action="store_true",
+                    help="run only the FMA and tensor-core peak microbenchmarks (one JSON line)")
     ap.add_argument("--ladder", action="store_true",
                     help="time the labelled ladder suite (pages' optimisation steps) instead")
     ap.add_argument("--simt-config", type=int, default=0,
@@ -697,6 +706,11 @@ def main(argv=None):
         return run_reference(args, ctx)
     if args.ladder:
         return run_ladder(args)
+    if args.peaks_only:
+        import torch
+        torch.cuda.set_device(0)
+        print(json.dumps(measure_peaks(0, load_peaks()[0]["sm_max_mhz"])))
+        return 0
     if args.configs:
         return run_configs(args)
 

@@ -320,61 +320,113 @@ __global__ void __launch_bounds__(256) k_cp_async(const float *__restrict__ A, c
 }
 
 // ---------------------------------------------------------------- PMPP
-// Corner turning: 16x16 tiles; A row-major, B column-major (element (k, j)
-// at B[j*K + k]), C row-major.  Consecutive threads (threadIdx.x) load
-// consecutive k of one B column, i.e. contiguous memory; the tile is stored
-// with the column index first and read transposed from shared memory.
-__global__ void __launch_bounds__(256) k_pmpp_corner_turn(const float *__restrict__ A,
-                                                          const float *__restrict__ Bcol,
-                                                          float *__restrict__ C, int M, int N, int K)
-{
-    constexpr int T = 16;
-    __shared__ float As[T][T];
-    __shared__ float Bs[T][T];  // Bs[column][k]
-    const int tx = threadIdx.x, ty = threadIdx.y;
-    const int row = blockIdx.y * T + ty, col = blockIdx.x * T + tx;
-    float acc = 0.0f;
-    for (int k0 = 0; k0 < K; k0 += T) {
-        As[ty][tx] = (row < M && k0 + tx < K) ? A[(long long)row * K + k0 + tx] : 0.0f;
-        const int bcol = blockIdx.x * T + ty, bk = k0 + tx;  // roles of tx and ty swapped
-        Bs[ty][tx] = (bcol < N && bk < K) ? Bcol[(long long)bcol * K + bk] : 0.0f;
-        __syncthreads();
-#pragma unroll
-        for (int kk = 0; kk < T; ++kk) acc = fmaf(As[ty][kk], Bs[tx][kk], acc);
-        __syncthreads();
-    }
-    if (row < M && col < N) C[(long long)row * N + col] = acc;
-}
-
-// Thread coarsening: 32x32 tiles; each block computes CF horizontally
-// adjacent output tiles and loads each A tile once for all of them.  M, K
-// multiples of 32, N a multiple of 32 * CF.
-template <int CF>
-__global__ void __launch_bounds__(1024) k_pmpp_coarsened(const float *__restrict__ A, const float *__restrict__ B,
+// The two worked examples of "PMPP Chapter 06: Performance considerations",
+// written from the section 1 and section 3 traffic analysis: what fixes
+// their global traffic is which tiles a block brings into shared memory and
+// how often, so each kernel below loads every element of its tiles exactly
+// once per phase, with consecutive lanes on consecutive addresses; the
+// thread-to-output mapping is this file's own.
+//
+// Corner turning (section 1): B is column-major (element (k, j) at
+// B[j*K + k]), so its contiguous direction is k.  A 64-thread block owns a
+// 16 x 16 tile of C.  Per 16-wide phase along K it loads the 16 x 16 tile of
+// A and of B by element index e = thread + 64*i: element e is (row e/16,
+// k e%16) of A and (column e/16, k e%16) of B, so lanes 0-15 of a warp read
+// 16 consecutive floats of one row of A or one column of B (coalesced for
+// both).  B is stored into shared memory transposed, Bt[k][column] (the
+// turn: the transpose happens between the coalesced global read and the
+// shared-memory write, not in the global access), and each thread then
+// computes a 2 x 2 block of C from two rows of A and two columns of Bt.
+// Global loads: 2*16*16 floats per block-phase, i.e. 8*m*n*k/16 bytes.
+__global__ void __launch_bounds__(64) k_pmpp_corner_turn(const float *__restrict__ A,
+                                                         const float *__restrict__ Bcol,
                                                          float *__restrict__ C, int M, int N, int K)
 {
-    constexpr int T = 32;
-    __shared__ float As[T][T];
-    __shared__ float Bs[T][T];
-    const int tx = threadIdx.x, ty = threadIdx.y;
-    const int row = blockIdx.y * T + ty;
-    const int col_first = blockIdx.x * T * CF + tx;
-    float acc[CF];
-#pragma unroll
-    for (int c = 0; c < CF; ++c) acc[c] = 0.0f;
+    constexpr int T = 16;
+    __shared__ float As[T][T + 1];  // [row][k]; the pad keeps column walks conflict-free
+    __shared__ float Bt[T][T + 1];  // [k][column]
+    const int t = threadIdx.x;
+    const int m0 = blockIdx.y * T, n0 = blockIdx.x * T;
+    const int r = 2 * (t >> 3), c = 2 * (t & 7);  // this thread's 2 x 2 block of the tile
+    float c00 = 0.0f, c01 = 0.0f, c10 = 0.0f, c11 = 0.0f;
     for (int k0 = 0; k0 < K; k0 += T) {
-        As[ty][tx] = A[(long long)row * K + k0 + tx];
 #pragma unroll
-        for (int c = 0; c < CF; ++c) {
-            Bs[ty][tx] = B[(long long)(k0 + ty) * N + col_first + c * T];
-            __syncthreads();
-#pragma unroll
-            for (int kk = 0; kk < T; ++kk) acc[c] = fmaf(As[ty][kk], Bs[kk][tx], acc[c]);
-            __syncthreads();
+        for (int i = 0; i < 4; ++i) {
+            const int e = t + 64 * i, outer = e >> 4, kk = e & 15;
+            const int gk = k0 + kk;
+            const int gm = m0 + outer, gn = n0 + outer;
+            As[outer][kk] = (gm < M && gk < K) ? A[(long long)gm * K + gk] : 0.0f;
+            Bt[kk][outer] = (gn < N && gk < K) ? Bcol[(long long)gn * K + gk] : 0.0f;
         }
-    }
+        __syncthreads();
 #pragma unroll
-    for (int c = 0; c < CF; ++c) C[(long long)row * N + col_first + c * T] = acc[c];
+        for (int kk = 0; kk < T; ++kk) {
+            const float a0 = As[r][kk], a1 = As[r + 1][kk];
+            const float b0 = Bt[kk][c], b1 = Bt[kk][c + 1];
+            c00 = fmaf(a0, b0, c00);
+            c01 = fmaf(a0, b1, c01);
+            c10 = fmaf(a1, b0, c10);
+            c11 = fmaf(a1, b1, c11);
+        }
+        __syncthreads();
+    }
+    const int gm = m0 + r, gn = n0 + c;
+    if (gm < M) {
+        if (gn < N) C[(long long)gm * N + gn] = c00;
+        if (gn + 1 < N) C[(long long)gm * N + gn + 1] = c01;
+    }
+    if (gm + 1 < M) {
+        if (gn < N) C[(long long)(gm + 1) * N + gn] = c10;
+        if (gn + 1 < N) C[(long long)(gm + 1) * N + gn + 1] = c11;
+    }
+}
+
+// Thread coarsening (section 3), tile width T = 32, coarsening factor CF:
+// a 256-thread block owns CF horizontally adjacent 32 x 32 tiles of C (a
+// 32 x 32*CF strip).  Per phase it loads the strip's one A tile once and its
+// CF B tiles, by element index (consecutive lanes along k for A, along the
+// columns for B: both coalesced), then synchronises once.  Thread t owns
+// row t/8 of the strip and the 4*CF columns (t%8) + 8*j: every A value it
+// reads from shared memory serves 4*CF multiply-adds across all CF tiles.
+// Global loads per block-phase: 32*32*(1 + CF) floats, i.e.
+// 4*m*n*k*(1 + 1/CF)/32 bytes in total.  M, K multiples of 32, N a multiple
+// of 32*CF.
+template <int CF>
+__global__ void __launch_bounds__(256) k_pmpp_coarsened(const float *__restrict__ A, const float *__restrict__ B,
+                                                        float *__restrict__ C, int M, int N, int K)
+{
+    constexpr int T = 32, W = T * CF;
+    __shared__ float As[T][T + 1];  // [row][k]
+    __shared__ float Bs[T][W];      // [k][column of the strip]
+    const int t = threadIdx.x;
+    const int m0 = blockIdx.y * T, n0 = blockIdx.x * W;
+    const int row = t >> 3, lane_col = t & 7;
+    float acc[4 * CF];
+#pragma unroll
+    for (int j = 0; j < 4 * CF; ++j) acc[j] = 0.0f;
+    for (int k0 = 0; k0 < K; k0 += T) {
+#pragma unroll
+        for (int i = 0; i < T * T / 256; ++i) {
+            const int e = t + 256 * i;
+            As[e >> 5][e & 31] = A[(long long)(m0 + (e >> 5)) * K + k0 + (e & 31)];
+        }
+#pragma unroll
+        for (int i = 0; i < T * W / 256; ++i) {
+            const int e = t + 256 * i;
+            Bs[e / W][e % W] = B[(long long)(k0 + e / W) * N + n0 + e % W];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < T; ++kk) {
+            const float a = As[row][kk];
+#pragma unroll
+            for (int j = 0; j < 4 * CF; ++j) acc[j] = fmaf(a, Bs[kk][lane_col + 8 * j], acc[j]);
+        }
+        __syncthreads();
+    }
+    float *crow = C + (long long)(m0 + row) * N + n0 + lane_col;
+#pragma unroll
+    for (int j = 0; j < 4 * CF; ++j) crow[8 * j] = acc[j];
 }
 
 bool aligned16(const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
@@ -392,8 +444,8 @@ extern "C" const char *gemm_ladder_name(int step)
     case GEMM_LADDER_WARP_TILING: return "6 warp tiling (4x8)";
     case GEMM_LADDER_DOUBLE_BUFFER: return "7 double buffering";
     case GEMM_LADDER_CP_ASYNC: return "8 cp.async 3-stage pipeline";
-    case GEMM_LADDER_PMPP_CORNER_TURN: return "PMPP corner turning (16x16, B column-major)";
-    case GEMM_LADDER_PMPP_COARSENED: return "PMPP thread coarsening (32x32, factor 4)";
+    case GEMM_LADDER_PMPP_CORNER_TURN: return "PMPP corner turning (16x16 tiles, B column-major, 2x2 per thread)";
+    case GEMM_LADDER_PMPP_COARSENED: return "PMPP thread coarsening (32x32 tiles, factor 4, 16 outputs per thread)";
     default: return "";
     }
 }
@@ -437,11 +489,11 @@ extern "C" int gemm_ladder_run(int step, int64_t M, int64_t N, int64_t K, const 
         k_cp_async<<<dim3(n / 128, m / 128), 256, 0, stream>>>(A, B, C, m, n, k);
         break;
     case GEMM_LADDER_PMPP_CORNER_TURN:
-        k_pmpp_corner_turn<<<dim3((n + 15) / 16, (m + 15) / 16), dim3(16, 16), 0, stream>>>(A, B, C, m, n, k);
+        k_pmpp_corner_turn<<<dim3((n + 15) / 16, (m + 15) / 16), 64, 0, stream>>>(A, B, C, m, n, k);
         break;
     case GEMM_LADDER_PMPP_COARSENED:
         if (M % 32 || K % 32 || N % 128) return GEMM_ERR_INVALID;
-        k_pmpp_coarsened<4><<<dim3(n / 128, m / 32), dim3(32, 32), 0, stream>>>(A, B, C, m, n, k);
+        k_pmpp_coarsened<4><<<dim3(n / 128, m / 32), 256, 0, stream>>>(A, B, C, m, n, k);
         break;
     default:
         return GEMM_ERR_INVALID;

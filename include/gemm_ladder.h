@@ -36,8 +36,8 @@ extern "C" {
 #define GEMM_LADDER_WARP_TILING 6      /* + 4x8 lanes per warp */
 #define GEMM_LADDER_DOUBLE_BUFFER 7    /* + two shared buffers, register prefetch */
 #define GEMM_LADDER_CP_ASYNC 8         /* + cp.async 3-stage pipeline */
-#define GEMM_LADDER_PMPP_CORNER_TURN 101 /* 16x16 tiles, column-major B loaded along K */
-#define GEMM_LADDER_PMPP_COARSENED 102   /* 32x32 tiles, 4 output tiles per block */
+#define GEMM_LADDER_PMPP_CORNER_TURN 101 /* 16x16 tiles, column-major B read along K, turned in shared memory */
+#define GEMM_LADDER_PMPP_COARSENED 102   /* 32x32 tiles, 4 output tiles per block (one A tile per phase) */
 
 /* Run one kernel of the suite.  Returns GEMM_OK or a GEMM_ERR_* code. */
 int gemm_ladder_run(int step, int64_t M, int64_t N, int64_t K, const float *A, const float *B,

@@ -67,3 +67,17 @@ def test_ladder_steps_agree_on_integer_inputs(oracle_mod):
     Cr, _ = oracle_mod.gemm(to_f64(A), to_f64(B), inp.B_ROW_MAJOR)
     for step in [1, 2, 3, 4, 5, 6, 7, 8]:
         assert np.array_equal(to_f64(_run(step, A, B, M, N, K)), Cr), step
+
+
+def test_pmpp_kernels_exact_on_integer_inputs(oracle_mod):
+    """Integer inputs make every sum exact: the corner-turning kernel (on the
+    column-major copy of B, ragged sizes) and the coarsening kernel equal the
+    oracle bit for bit."""
+    M, N, K = 200, 136, 130
+    A, Bc = inp.make_integer_operands(M, N, K, layout_b=inp.B_COL_MAJOR, seed=5)
+    Cr, _ = oracle_mod.gemm(to_f64(A), to_f64(Bc), inp.B_COL_MAJOR)
+    assert np.array_equal(to_f64(_run(101, A, Bc, M, N, K)), Cr)
+    M, N, K = 96, 384, 96
+    A, B = inp.make_integer_operands(M, N, K, seed=6)
+    Cr, _ = oracle_mod.gemm(to_f64(A), to_f64(B), inp.B_ROW_MAJOR)
+    assert np.array_equal(to_f64(_run(102, A, B, M, N, K)), Cr)
