@@ -37,6 +37,9 @@ METRIC = "GEMM TFLOPS (2MNK/t) and % of GB300 FP32-SIMT / tensor-core roofline"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "fp32_8192_row"
 TC_WORKLOADS = ["ffn_bf16_8192x14336x4096", "ffn_tf32_8192x14336x4096", "fp32x3_8192_row"]
+# Bursts in which a workload's timed steps alternate with the cuBLAS side
+# reference's (same count), when the side reference is measured.
+SIDE_ROUNDS = 5
 # The other specified FP32 workloads, measured under "modes" too.
 SIMT_WORKLOADS = ["fp32_128_row", "fp32_1024_colB", "fp32_4095x3073x2047_row"]
 # Modes whose step is short run at least this many timed steps (recorded in
@@ -260,9 +263,35 @@ def bench_workload(g, name, steps, warmup, dist_ctx, peaks, peak_note, with_e2e,
     def run():
         g.run(A_d, B_d, C_d, w.layout_b, w.dtype, stream)
 
+    cub = None
+    if side_cublas:
+        # Labelled side reference: cuBLAS through torch on the same operands.
+        # Never part of this library's path.  Its steps are interleaved with
+        # this library's in SIDE_ROUNDS bursts, so both see the same power
+        # and thermal state (timed one after the other, the second one ran
+        # in a hotter GPU and the comparison depended on the order).
+        torch.backends.cuda.matmul.allow_tf32 = w.dtype == "tf32"
+        Bl = B_d if w.layout_b == 0 else B_d.t()
+        cub_fn, cub_what = cublas_side_call(A_d, Bl, w.dtype)
     barrier(dist_ctx)
     t0 = time.time()
-    total_ms, per, launches = time_device(run, stream, steps, warmup, lambda: g.launch_count)
+    if side_cublas:
+        per_round = max(1, steps // SIDE_ROUNDS)
+        steps = per_round * SIDE_ROUNDS
+        for _ in range(warmup):
+            cub_fn()
+        total_ms, per, launches, cub_ms = 0.0, [], 0, 0.0
+        for r in range(SIDE_ROUNDS):
+            tm, pr, ln = time_device(run, stream, per_round, warmup if r == 0 else 0, lambda: g.launch_count)
+            total_ms, per, launches = total_ms + tm, per + pr, launches + ln
+            ctm, _, _ = time_device(cub_fn, stream, per_round, 0)
+            cub_ms += ctm
+        torch.backends.cuda.matmul.allow_tf32 = False
+        cub = {"tflops": w.flops / (cub_ms / steps * 1e-3) / 1e12,
+               "what": "cuBLAS through torch on the same operands; " + cub_what,
+               "steps": steps, "interleaved_rounds": SIDE_ROUNDS}
+    else:
+        total_ms, per, launches = time_device(run, stream, steps, warmup, lambda: g.launch_count)
     t1 = time.time()
     g.sync_status(stream)
     barrier(dist_ctx)
@@ -288,22 +317,12 @@ def bench_workload(g, name, steps, warmup, dist_ctx, peaks, peak_note, with_e2e,
         "M": w.M, "N": w.N, "K": w.K, "layout_b": "row" if w.layout_b == 0 else "col",
         "dtype": w.dtype, "value": value, "ms_per_step": ms_max, "kernel_ms": kernel_ms,
         "kernel_ms_min": min(per), "kernel_ms_median": statistics.median(per),
-        "path": g.last_path, "roofline": roof,
+        "path": g.last_path, "roofline": roof, "steps": steps,
         "launches_timed": launches, "wall_window": (t0, t1),
         "compulsory_bytes": rl.compulsory_bytes(w.M, w.N, w.K, es),
     }
-    if side_cublas:
-        # Labelled side reference: cuBLAS through torch on the same operands,
-        # same stream and power state.  Never part of this library's path.
-        torch.backends.cuda.matmul.allow_tf32 = w.dtype == "tf32"
-        Bl = B_d if w.layout_b == 0 else B_d.t()
-        fn, what = cublas_side_call(A_d, Bl, w.dtype)
-        cub_ms, _, _ = time_device(fn, stream, max(5, steps // 2), warmup)
-        torch.backends.cuda.matmul.allow_tf32 = False
-        res["cublas_side"] = {
-            "tflops": w.flops / (cub_ms / max(5, steps // 2) * 1e-3) / 1e12,
-            "what": "cuBLAS through torch on the same operands; " + what,
-        }
+    if cub is not None:
+        res["cublas_side"] = cub
     if with_e2e:
         Ah = A.pin_memory()
         Bh = B.pin_memory()
@@ -483,6 +502,8 @@ def apply_options(g, args):
         g.set_option(gemm.GEMM_OPT_TC_CLUSTER, args.tc_mode)
     if args.split_k:
         g.set_option(gemm.GEMM_OPT_SPLIT_K, args.split_k)
+    if args.tc_group_m:
+        g.set_option(gemm.GEMM_OPT_TC_GROUP_M, args.tc_group_m)
 
 
 def run_configs(args):
@@ -681,6 +702,8 @@ def main(argv=None):
                     help="force the FP32 tile configuration (GEMM_OPT_SIMT_CONFIG; 0 = chosen per shape)")
     ap.add_argument("--tc-mode", type=int, default=0,
                     help="force the tensor-core mode (GEMM_OPT_TC_CLUSTER: 1 one CTA per tile, 3 pair MMA; 0 = default)")
+    ap.add_argument("--tc-group-m", type=int, default=0,
+                    help="GEMM_OPT_TC_GROUP_M: tensor-core tile-order group height in units (0 = chosen)")
     ap.add_argument("--split-k", type=int, default=0,
                     help="GEMM_OPT_SPLIT_K (0 = chosen per shape, 1 = never, n = n slices)")
     ap.add_argument("--results", default=None,
@@ -759,7 +782,7 @@ def main(argv=None):
                                with_e2e=False, side_cublas=not args.no_side_reference)
             m = {k: r[k] for k in ("workload", "description", "dtype", "value",
                                    "ms_per_step", "kernel_ms", "kernel_ms_median", "path", "roofline")}
-            m["steps"], m["warmup"] = mode_steps, args.warmup
+            m["steps"], m["warmup"] = r["steps"], args.warmup
             m["l2"] = l2_note(r)
             if r["dtype"] == "f32" and measured:
                 add_microbench(m["roofline"], max(measured.get("ffma_tflops") or 0.0,
