@@ -701,3 +701,54 @@ def test_workload_ragged_4095x3073x2047(g, oracle_mod, elementwise):
                                   "ffn_tf32_8192x14336x4096"])
 def test_workload_sampled(g, oracle_mod, name):
     _sampled_check(g, oracle_mod, inp.WORKLOADS[name])
+
+
+def _odd_pitch(t, dev):
+    """t on dev with a row pitch of cols + 1 elements (not a multiple of 16
+    bytes), so the library re-packs it into the handle's workspace."""
+    rows, cols = t.shape
+    buf = torch.zeros((rows, cols + 1), dtype=t.dtype, device=dev)
+    buf[:, :cols] = t.to(dev)
+    return buf[:, :cols]
+
+
+def test_workspace_grows_in_stream_order(oracle_mod):
+    """A fresh handle's workspace grows while earlier calls that use it are
+    still queued: small re-packed call, a larger one that must grow the
+    workspace, and the small one again, back to back on one stream with no
+    host synchronisation; then a larger call on a second stream ordered
+    after the first by an event.  Every result matches the oracle."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dense_gemm_sm100_gb300 import gemm
+    dev = torch.device("cuda", 0)
+    shapes = [(300, 260, 130), (1100, 900, 700), (300, 260, 130)]
+    with gemm.Gemm(0) as h:
+        s1 = torch.cuda.Stream()
+        ops, outs = [], []
+        for i, (M, N, K) in enumerate(shapes):
+            A, B = inp.make_integer_operands(M, N, K, seed=40 + i)
+            ops.append((A, B))
+            with torch.cuda.stream(s1):
+                A_d, B_d = _odd_pitch(A, dev), _odd_pitch(B, dev)
+                C = torch.full((M, N), float("nan"), device=dev)
+                h.run(A_d, B_d, C, ROW, "f32", s1)
+                outs.append((A_d, B_d, C))
+        assert "+repackA" in h.last_path
+        ev = torch.cuda.Event()
+        ev.record(s1)
+        s2 = torch.cuda.Stream()
+        s2.wait_event(ev)
+        M, N, K = 1500, 1300, 900
+        A, B = inp.make_integer_operands(M, N, K, seed=49)
+        ops.append((A, B))
+        with torch.cuda.stream(s2):
+            A_d, B_d = _odd_pitch(A, dev), _odd_pitch(B, dev)
+            C = torch.full((M, N), float("nan"), device=dev)
+            h.run(A_d, B_d, C, ROW, "f32", s2)
+            outs.append((A_d, B_d, C))
+        h.sync_status(s2)
+        torch.cuda.synchronize()
+    for (A, B), (_, _, C) in zip(ops, outs):
+        Cr, _ = oracle_of(oracle_mod, A, B, ROW)
+        assert np.array_equal(to_f64(C), Cr)
