@@ -564,6 +564,14 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
 #pragma unroll
             for (int j = 0; j < TN / 2; ++j) acc2[i][j] = make_float2(0.0f, 0.0f);
 
+        // A warp whose rows (or columns) of this tile all lie outside C has
+        // no multiply-adds to do (the last tile row of 8192 rows in 192-row
+        // tiles holds 128 real rows; the last tile column of N = 3073 in
+        // 128-column tiles one): it only releases each stage, and the other
+        // warps of its scheduler get the FMA pipe.
+        const bool idle = (long long)mb * BM + (wm >> 1) * 64 + (wm & 1) * 4 >= p.M ||
+                          (long long)nb * BN + wn * 8 * TN >= p.N;
+
         for (int kt = w.kt_begin; kt < w.kt_end; ++kt, ++it) {
             const uint32_t s = it % STAGES;
             const uint32_t ph = (it / STAGES) & 1u;
@@ -574,7 +582,8 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
                                             kWaitConsumerFull, p.timeout_ns))
                 return;
             const uint8_t *st = smem + s * STAGE_BYTES;
-            if (S::PINGPONG) {
+            if (idle) {
+            } else if (S::PINGPONG) {
                 // Fragment double buffering ("GEMM 性能优化", 台阶 6, p-Loop
                 // level): the A fragments of k group g+1 and the B fragment of
                 // row k+1 are loaded while row k is multiplied.  The packed
