@@ -891,17 +891,20 @@ void launch_cfg(int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB, co
 // With the double-buffered, column-pair-major inner loop (8 x 8 thread
 // tiles): 192x128 with 12 consumer warps 70.3 row-major / 67.1 column-major
 // B, 128x128 with 8 consumer warps 69.0 / 63.5.  16 consumer warps of 8 x 4
-// (128x128w16, A loaded in pairs, row-pair-major order) 66.6 row-major.  The
-// scalar-FMA, 64x128 and 64x64 tiles (56.4, 59.2 and 31.5 at 8192^3 before
-// the new inner loop), 128x256 with register reallocation (8x16 per thread,
-// 64.0) and 16 consumer warps of 8x8 with A loaded in pairs (256x128, 112
-// registers, spills: 59.3) never win; they stay selectable.  With scalar
-// FMAs instead of packed pairs the 192x128 tile is issue-bound (57.7).
+// (128x128w16, A loaded in pairs, row-pair-major order) 66.6 row-major.
+// 64x128 (4 consumer warps) 58.9 / 51.4 and 64x64 (2) 31.5 / 29.3: they win
+// only where a problem is a few tiles (128^3: 64x64 11.9 us per call against
+// 14.4 for one 128x128 tile), because a CTA's serial work shrinks with its
+// tile.  The scalar-FMA tile (56.4 at 8192^3 before the new inner loop),
+// 128x256 with register reallocation (8x16 per thread, 64.0) and 16 consumer
+// warps of 8x8 with A loaded in pairs (256x128, 112 registers, spills: 59.3)
+// never win; they stay selectable.  With scalar FMAs instead of packed pairs
+// the 192x128 tile is issue-bound (57.7).
 ConfigEntry g_configs[] = {
     DG_SIMT_CFG(4, 2, 8, 6, 8, 1, 0, 69.0f, 63.5f, "128x128"),
     DG_SIMT_CFG(4, 2, 8, 6, 8, 0, 0, 0.0f, 0.0f, "128x128s"),
-    DG_SIMT_CFG(2, 2, 8, 4, 8, 1, 0, 0.0f, 0.0f, "64x128"),
-    DG_SIMT_CFG(2, 1, 8, 4, 8, 1, 0, 0.0f, 0.0f, "64x64"),
+    DG_SIMT_CFG(2, 2, 8, 4, 8, 1, 0, 58.9f, 51.4f, "64x128"),
+    DG_SIMT_CFG(2, 1, 8, 4, 8, 1, 0, 31.5f, 29.3f, "64x64"),
     DG_SIMT_CFG(4, 2, 16, 4, 8, 1, 1, 0.0f, 0.0f, "128x256r"),
     DG_SIMT_CFG(6, 2, 8, 4, 8, 1, 1, 70.3f, 67.1f, "192x128r"),
     DG_SIMT_CFG(4, 4, 4, 6, 8, 1, 1, 66.6f, 0.0f, "128x128w16"),
