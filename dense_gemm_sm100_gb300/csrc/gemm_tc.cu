@@ -25,6 +25,7 @@
 // so no transpose pass is needed.  MN-major TF32 tiles are staged with the
 // 32-byte-atom variant of the 128-byte swizzle.  Out-of-range elements are
 // zero-filled by TMA and stores are guarded, so any M, N, K works.
+#include <algorithm>
 #include <cstdint>
 
 #include "../../include/gemm.h"
@@ -858,11 +859,17 @@ cudaError_t launch_tc(int dtype, int layout_b, const CUtensorMap &tmA, const CUt
     p.kt_per_split = split ? sp.kt_per_split : (K + (128 / (dtype == GEMM_BF16 ? 2 : 4)) - 1) / (128 / (dtype == GEMM_BF16 ? 2 : 4));
     if (p.kt_per_split < 1) p.kt_per_split = 1;
     p.partials = split ? sp.partials : nullptr;
-    // 500 ns between chunks delays the TMEM release by at most 3.5 us; a tile
-    // of 32 or more 128-byte K stages lasts longer than that at full rate.
-    // FFN BF16 8192x14336x4096: +1 % on one box (TF32 unchanged), within
-    // the run-to-run spread on another, interleaved runs.
-    p.epi_pace_ns = cl == 3 && !split && p.kt_per_split >= 32 ? 500u : 0u;
+    // The epilogue spaces a tile's 8 C chunks 25 ns per ring stage of the
+    // tile apart, at most 1 us (FFN shape: 1 us), which delays the TMEM
+    // release by 7 spacings: at most 5.6 us for the shortest paced tile (32
+    // stages, about 9 us of MMAs), so the MMA warp never waits for it.  C
+    // writes cost the FFN shape 8 % (BF16) against a copy that skips them;
+    // spread over the tile they cost less: interleaved on one box, BF16 /
+    // TF32 TFLOP/s 1915 / 995 unpaced, 1925 / 989 at 500 ns, 1941 / 1000 at
+    // 1 us, 1917 / 994 at 2 us; at 4 us the release came too late (1342).
+    p.epi_pace_ns = cl == 3 && !split && p.kt_per_split >= 32
+                        ? static_cast<unsigned>(std::min(1000, 25 * p.kt_per_split))
+                        : 0u;
     const CUtensorMap &tc = tmC != nullptr ? *tmC : tmA;  // unused when c_tma == 0
     const bool bf16 = dtype == GEMM_BF16;
     if (cl == 3 && wide) {
