@@ -37,6 +37,7 @@ struct gemm_ctx {
     int elementwise = 0;  // FP32 unaligned operands: element-wise producer (1) or re-pack (0)
     size_t ws_limit = 0;  // 0: none; else the workspace never grows beyond this many bytes
     int split_k = 0;      // 0: chosen per shape; 1: never; n > 1: n K slices (FP32 path)
+    int stream_k = 0;     // FP32 tail: 0 chosen per shape, 1 slices, 2 stream-K
     int tc_cluster = 3;   // tensor-core mode: 1 one CTA per tile, 3 pair MMA
     int tc_tma_store = 1; // tensor-core epilogue writes C with TMA stores when C allows it
     int tc_slices = 0;    // pair MMA: K slices per ring stage (0: library's choice)
@@ -185,7 +186,9 @@ PackPlan plan_pack(const gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_
         const dg::SimtTile t = dg::simt_tile(pp.simt_config, layout_b);
         if (h->split_k == 0) {
             const int64_t slots = h->max_ctas > 0 ? h->max_ctas : int64_t{h->sm_count} * t.ctas_per_sm;
-            pp.split = dg::simt_pick_splits(pp.simt_config, layout_b, M, N, K, slots);
+            // the element-wise producer has no stream-K form
+            pp.split = dg::simt_pick_splits(pp.simt_config, layout_b, M, N, K, slots,
+                                            pp.elementwise ? 1 : h->stream_k);
         } else if (h->split_k > 1) {  // every tile in split_k slices
             const int64_t tiles = ((M + t.bm - 1) / t.bm) * ((N + t.bn - 1) / t.bn);
             pp.split = dg::simt_split_k(tiles, tiles, h->split_k, K);
@@ -397,7 +400,7 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
             if (rc) return rc;
         }
         dg::SplitK sk = pp.split;
-        if (sk.splits > 1) sk.partials = reinterpret_cast<float *>(ws + pp.a_bytes + pp.b_bytes);
+        if (sk.active()) sk.partials = reinterpret_cast<float *>(ws + pp.a_bytes + pp.b_bytes);
         const int64_t units = dg::simt_units(cfg, layout_b, M, N, sk);
         const int64_t cap = h->max_ctas > 0 ? h->max_ctas : int64_t{h->sm_count} * t.ctas_per_sm;
         lc.grid = static_cast<int>(units < cap ? units : cap);
@@ -411,14 +414,17 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
                                       static_cast<int>(K), C, ldc, c_vec4, lc, sk);
         if (e != cudaSuccess) return cuda_fail(h, e, "FP32 SIMT kernel launch");
         path = std::string("simt_f32_") + t.name + "_" + lay + (pp.elementwise ? "+cpasync" : "") + path;
-        if (sk.splits > 1) {
+        if (sk.active()) {
             ++h->launches;
             e = dg::launch_simt_tail_reduce(cfg, layout_b, static_cast<int>(M), static_cast<int>(N),
                                             static_cast<int>(K), C, ldc, c_vec4, lc, sk, h->sm_count);
             if (e != cudaSuccess) return cuda_fail(h, e, "split-K reduction launch");
             const int64_t tiles = ((M + t.bm - 1) / t.bm) * ((N + t.bn - 1) / t.bn);
-            path += sk.tail_tiles == tiles ? "+splitk" + std::to_string(sk.splits)
-                                           : "+tail" + std::to_string(sk.tail_tiles) + "x" + std::to_string(sk.splits);
+            if (sk.stream_k)
+                path += "+streamk" + std::to_string(sk.tail_tiles) + "on" + std::to_string(sk.sk_parts);
+            else
+                path += sk.tail_tiles == tiles ? "+splitk" + std::to_string(sk.splits)
+                                               : "+tail" + std::to_string(sk.tail_tiles) + "x" + std::to_string(sk.splits);
         }
     } else {
         const int bk = dg::tc_bk(es);
@@ -910,6 +916,10 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value)
     case GEMM_OPT_SPLIT_K:
         if (value < 0 || value > 64) break;
         h->split_k = static_cast<int>(value);
+        return GEMM_OK;
+    case GEMM_OPT_STREAM_K:
+        if (value < 0 || value > 2) break;
+        h->stream_k = static_cast<int>(value);
         return GEMM_OK;
     default:
         return fail(h, GEMM_ERR_INVALID, "unknown option");

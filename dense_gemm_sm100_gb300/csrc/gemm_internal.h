@@ -19,14 +19,31 @@ struct SimtTile {
     const char *name;
 };
 
-// Split of K into slices for the tail of the tile order: the last
-// tail_tiles tiles (all of them for a uniform split) are each computed as
-// `splits` partial tiles that are summed afterwards.
+// Split of K for the tail of the tile order: the last tail_tiles tiles (all
+// of them for a uniform split) are computed as partial tiles that a second
+// kernel sums.  Two forms:
+//  * slices (stream_k == 0): each tail tile is cut into `splits` K slices of
+//    k_per_split elements; partial tile (slice, tail tile r) at slot
+//    slice * tail_tiles + r;
+//  * stream-K (stream_k == 1): the tail tiles' k-tile iterations, tile after
+//    tile, are cut into sk_parts equal contiguous ranges, one for each of the
+//    first sk_parts persistent CTAs (the launch grid must be sk_ctas; there
+//    are fewer parts than CTAs only when there are fewer than four k-tiles
+//    per CTA); a range that crosses a tile boundary yields one segment per
+//    tile it touches.
+//    Segment j (in k order) of tail tile r goes to slot r * sk_smax + j.
+//    k_per_split holds the longest range, in elements.
 struct SplitK {
-    int splits = 1;             // 1 = no split: every tile writes C directly
-    int k_per_split = 0;        // elements of K per slice (multiple of kSimtBK)
-    int64_t tail_tiles = 0;     // tiles cut into slices
-    float *partials = nullptr;  // splits x tail_tiles tiles of bm x bn floats
+    int splits = 1;             // slices: 1 = no split, every tile writes C directly
+    int k_per_split = 0;        // slices: elements of K per slice (multiple of kSimtBK)
+    int64_t tail_tiles = 0;     // tiles cut into slices / segments
+    int stream_k = 0;           // 1: stream-K segments instead of equal slices
+    int64_t sk_ctas = 0;        // stream-K: CTAs of the launch grid
+    int64_t sk_parts = 0;       // stream-K: CTAs with a range, min(sk_ctas, iterations / 4), at least 1
+    int64_t sk_smax = 0;        // stream-K: most segments of one tile (slots per tile)
+    float *partials = nullptr;  // partial tiles of bm x bn floats
+    bool active() const { return tail_tiles > 0 && (stream_k ? sk_parts > 0 : splits > 1); }
+    int64_t partial_tiles() const { return !active() ? 0 : stream_k ? tail_tiles * sk_smax : splits * tail_tiles; }
 };
 
 int simt_num_configs();
@@ -35,12 +52,21 @@ SimtTile simt_tile(int config, int layout_b);
 // capped at max_ctas CTAs when max_ctas > 0).
 int simt_pick_config(int64_t M, int64_t N, int64_t K, int layout_b, int sm_count, int max_ctas);
 bool simt_config_usable(int config);  // false if the device cannot run it
+bool simt_has_stream_k(int config);   // true if it has stream-K kernels (TMA-loaded operands)
 // K slices for the tiles of a partial last wave, on `slots` CTA slots.
-SplitK simt_pick_splits(int config, int layout_b, int64_t M, int64_t N, int64_t K, int64_t slots);
+// stream_k: 0 = slices or stream-K, whichever the wave model rates faster;
+// 1 = slices only; 2 = stream-K whenever there is a tail.  A configuration
+// without stream-K kernels always takes slices; so must a caller whose
+// operands go through the element-wise producer.
+SplitK simt_pick_splits(int config, int layout_b, int64_t M, int64_t N, int64_t K, int64_t slots,
+                        int stream_k = 0);
 // `want` slices (fewer if K is short) of the last `tail` of `tiles` tiles.
 SplitK simt_split_k(int64_t tiles, int64_t tail, int64_t want, int64_t K);
-// Work units of the persistent FP32 kernel, and the workspace its partial
-// tiles need.
+// Stream-K over the last `tail` of `tiles` tiles on `ctas` CTAs.
+SplitK simt_stream_k(int64_t tiles, int64_t tail, int64_t ctas, int64_t K);
+// Work units of the persistent FP32 kernel (the launch grid is at most
+// that; with stream-K it is exactly the grid the plan was made for), and
+// the workspace its partial tiles need.
 int64_t simt_units(int config, int layout_b, int64_t M, int64_t N, const SplitK &sk);
 size_t simt_partial_bytes(int config, int layout_b, const SplitK &sk);
 

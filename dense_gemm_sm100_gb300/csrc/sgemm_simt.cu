@@ -45,12 +45,31 @@ struct SimtParams {
     // Units [0, full_units) are whole tiles (tile order position = unit);
     // then the last tail_tiles tiles of the order, each cut into `splits` K
     // slices of k_per_split elements (a multiple of BK), whose partial tiles
-    // go to `partials` (slice-major, BM x BN floats each).
+    // go to `partials` (slice-major, BM x BN floats each).  splits == 0:
+    // stream-K (sk below) instead of slices.
     int full_units, tail_tiles, splits, k_per_split;
     float *partials;
-    // operands for the element-wise producer (LAYOUT_B == 3)
-    const float *A, *B;
-    long long lda, ldb;
+    // The element-wise producer (LAYOUT_B == 3) has no stream-K form, so its
+    // operands and the stream-K plan share the space: the parameter block
+    // stays at its size without stream-K (with 40 more bytes the
+    // column-major kernel ran 6 % slower, though it never read them).
+    union {
+        struct {
+            const float *A, *B;
+            long long lda, ldb;
+        } ew;
+        // Stream-K: units [base, base + kmax * ctas) are segment k = (u -
+        // base) / ctas of CTA c = (u - base) % ctas (the grid is ctas CTAs and
+        // base a multiple of it, so CTA c runs them); CTA c < parts owns the
+        // tail's k-tile iterations [c * iters / parts, (c + 1) * iters /
+        // parts), at least one each.  Units in [full_units, base), of CTAs
+        // c >= parts and segments past a CTA's range are empty.  A tail tile
+        // has k_tiles iterations and at most smax segments.
+        struct {
+            long long iters;
+            int parts, smax, base, kmax, ctas, k_tiles;
+        } sk;
+    };
     float *C;
     long long ldc;
     int *status;
@@ -58,6 +77,7 @@ struct SimtParams {
     int c_vec4;
     int debug_drop;  // test hook: CTA 0 never loads its first stage
 };
+static_assert(sizeof(SimtParams) == 120, "keep the parameter block at its measured size");
 
 // Work unit u (persistent loop index) -> output tile and K range; split < 0
 // means the whole K range, written to C.
@@ -78,12 +98,49 @@ __device__ __forceinline__ void tile_coords(int t, const SimtParams &p, int &mb,
     nb = r / gm;
 }
 
+// Stream-K: the CTA owning iteration x of the tail, the last c with
+// floor(c * I / P) <= x (P = sk_parts <= I, so every range is non-empty
+// and consecutive tiles' owners are consecutive CTAs).
+__device__ __forceinline__ long long sk_owner(long long x, const SimtParams &p)
+{
+    return ((x + 1) * p.sk.parts - 1) / p.sk.iters;
+}
+
+// Stream-K range of one CTA, worked out once per CTA (into shared memory)
+// so that a unit's coordinates take no 64-bit division: iterations
+// [lo, hi), tail tiles r0..r1 (r1 < r0: none), and the segment index of
+// its first piece within tile r0.  Every later piece starts its tile, so
+// it is that tile's segment 0.
+struct SkCta {
+    long long lo, hi;
+    int r0, r1, split0;
+};
+
+__device__ __forceinline__ SkCta sk_cta_range(int c, const SimtParams &p)
+{
+    SkCta r;
+    r.lo = r.hi = 0;
+    r.r0 = 0;
+    r.r1 = -1;
+    r.split0 = 0;
+    if (p.splits != 0 || c >= p.sk.parts) return r;
+    r.lo = (long long)c * p.sk.iters / p.sk.parts;
+    r.hi = (long long)(c + 1) * p.sk.iters / p.sk.parts;
+    r.r0 = static_cast<int>(r.lo / p.sk.k_tiles);
+    r.r1 = static_cast<int>((r.hi - 1) / p.sk.k_tiles);
+    r.split0 = static_cast<int>(c - sk_owner((long long)r.r0 * p.sk.k_tiles, p));
+    return r;
+}
+
 // Whole tiles first; the tail tiles run slice-major, so the slices of one
 // tile go to different CTAs of the last wave.  The K range of slice s is
 // [s*k_per_split, min(K, (s+1)*k_per_split)) ("GEMM 性能优化", 台阶 1:
 // partial sums over K slices add up to the product; Wave 模型: the last,
-// partial wave is spread over all CTAs).
-__device__ __forceinline__ Unit unit_coords(int u, const SimtParams &p)
+// partial wave is spread over all CTAs).  With stream-K every CTA gets an
+// equal share of the tail's k-tile iterations instead, cut at tile
+// boundaries into segments; a unit with kt_begin == kt_end is empty.
+template <bool SK>
+__device__ __forceinline__ Unit unit_coords(int u, const SimtParams &p, const SkCta &sc)
 {
     Unit w;
     if (u < p.full_units) {
@@ -92,6 +149,24 @@ __device__ __forceinline__ Unit unit_coords(int u, const SimtParams &p)
         w.kt_end = (p.K + kSimtBK - 1) / kSimtBK;
         w.split = -1;
         w.slot = 0;
+        return w;
+    }
+    if constexpr (SK) {
+        // u is a unit of this CTA (u = blockIdx.x + j * gridDim.x), whose
+        // range `sc` holds; its k-th segment unit covers tail tile r0 + k
+        w.mb = w.nb = 0;
+        w.kt_begin = w.kt_end = 0;
+        w.split = w.slot = 0;
+        if (u < p.sk.base) return w;
+        const int k = (u - p.sk.base) / p.sk.ctas;
+        const int r = sc.r0 + k;  // tail tile of this segment
+        if (r > sc.r1) return w;
+        const long long t0 = (long long)r * p.sk.k_tiles;
+        w.kt_begin = static_cast<int>((sc.lo > t0 ? sc.lo : t0) - t0);
+        w.kt_end = static_cast<int>((sc.hi < t0 + p.sk.k_tiles ? sc.hi : t0 + p.sk.k_tiles) - t0);
+        w.split = k == 0 ? sc.split0 : 0;  // segment index within the tile
+        w.slot = r * p.sk.smax + w.split;
+        tile_coords(p.full_units + r, p, w.mb, w.nb);
         return w;
     }
     const int v = u - p.full_units;
@@ -108,10 +183,15 @@ __device__ __forceinline__ Unit unit_coords(int u, const SimtParams &p)
 
 // Number of K stages (k-tiles) of work unit u, as unit_coords would give
 // (kt_end - kt_begin) without the tile coordinates.
-__device__ __forceinline__ int unit_stages(int u, const SimtParams &p)
+template <bool SK>
+__device__ __forceinline__ int unit_stages(int u, const SimtParams &p, const SkCta &sc)
 {
     const int k_tiles = (p.K + kSimtBK - 1) / kSimtBK;
     if (u < p.full_units) return k_tiles;
+    if constexpr (SK) {
+        const Unit w = unit_coords<SK>(u, p, sc);
+        return w.kt_end - w.kt_begin;
+    }
     const int split = (u - p.full_units) / p.tail_tiles;
     const int k0 = split * p.k_per_split;
     const int k1 = min(p.K, k0 + p.k_per_split);
@@ -183,7 +263,9 @@ struct Simt {
     static_assert(BM <= 256 && BN <= 256, "TMA box limit");
 };
 
-template <int LAYOUT_B, int WM, int WN, int TN, int STAGES, int GU, int F2, int PWG>
+// SK: the stream-K form (its own instantiation, so the main loop of the
+// other form is compiled exactly as without it).
+template <int LAYOUT_B, int WM, int WN, int TN, int STAGES, int GU, int F2, int PWG, bool SK>
 __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG>::THREADS, 1)
     sgemm_simt_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const SimtParams p)
@@ -207,7 +289,8 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int num_units = p.full_units + p.tail_tiles * p.splits;
+    const int num_units = SK ? p.sk.base + p.sk.kmax * p.sk.ctas : p.full_units + p.tail_tiles * p.splits;
+    __shared__ SkCta sk_cta;  // referenced only by the stream-K form
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -218,6 +301,7 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
             if (LAYOUT_B == 2) mbar_init(ready_bar + 8 * s, S::TURN_WARPS);  // every turning warp
         }
         *abort_flag = 0;
+        if constexpr (SK) sk_cta = sk_cta_range(blockIdx.x, p);
         fence_barrier_init();
     }
     __syncthreads();
@@ -245,7 +329,7 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
             uint32_t it = 0;
             bool ok = true;
             for (int unit = blockIdx.x; ok && unit < num_units; unit += gridDim.x) {
-                const Unit w = unit_coords(unit, p);
+                const Unit w = unit_coords<SK>(unit, p, sk_cta);
                 for (int kt = w.kt_begin; kt < w.kt_end; ++kt, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
@@ -264,7 +348,7 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
                         const long long m = (long long)w.mb * BM + r;
                         const bool in = m < p.M && k0 + kk < p.K;
                         const uint32_t dst = st + r * 128 + ((((kk >> 2) ^ (r & 7)) << 4) | ((kk & 3) << 2));
-                        cp_async_4(dst, in ? p.A + m * p.lda + k0 + kk : p.A, in ? 4u : 0u);
+                        cp_async_4(dst, in ? p.ew.A + m * p.ew.lda + k0 + kk : p.ew.A, in ? 4u : 0u);
                     }
                     for (int e = pt; e < BK * BN; e += PT) {
                         const int kk = e / BN, n = e - (e / BN) * BN;
@@ -272,7 +356,7 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
                         const bool in = col < p.N && k0 + kk < p.K;
                         const uint32_t dst = st + A_BYTES + (n >> 5) * 4096 + kk * 128 +
                                              (((((n & 31) >> 2) ^ (kk & 7)) << 4) | ((n & 3) << 2));
-                        cp_async_4(dst, in ? p.B + (long long)(k0 + kk) * p.ldb + col : p.B, in ? 4u : 0u);
+                        cp_async_4(dst, in ? p.ew.B + (long long)(k0 + kk) * p.ew.ldb + col : p.ew.B, in ? 4u : 0u);
                     }
                     cp_async_mbar_arrive_noinc(full_bar + 8 * s);
                 }
@@ -292,7 +376,7 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
             uint32_t it = 0;
             bool ok = true;
             for (int unit = blockIdx.x; ok && unit < num_units; unit += gridDim.x) {
-                const Unit w = unit_coords(unit, p);
+                const Unit w = unit_coords<SK>(unit, p, sk_cta);
                 for (int kt = w.kt_begin; kt < w.kt_end; ++kt, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
@@ -336,7 +420,7 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
             const int nq = 8 * tg + tt;  // rows 4*nq .. 4*nq + 3 of the B tile
             uint32_t it = 0;
             for (int unit = blockIdx.x; unit < num_units; unit += gridDim.x) {
-                const int stages = unit_stages(unit, p);
+                const int stages = unit_stages<SK>(unit, p, sk_cta);
                 for (int j = 0; j < stages; ++j, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
@@ -392,13 +476,17 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
             const bool issuer = pw == 0;
             uint32_t issued = 0;
             int iss_unit = blockIdx.x, iss_kt = 0, iss_kt_end = 0, iss_mb = 0, iss_nb = 0;
+            // the next unit of this CTA that has stages (stream-K units can be empty)
             auto iss_load_unit = [&]() {
-                if (iss_unit < num_units) {
-                    const Unit w = unit_coords(iss_unit, p);
-                    iss_mb = w.mb;
-                    iss_nb = w.nb;
-                    iss_kt = w.kt_begin;
-                    iss_kt_end = w.kt_end;
+                for (; iss_unit < num_units; iss_unit += gridDim.x) {
+                    const Unit w = unit_coords<SK>(iss_unit, p, sk_cta);
+                    if (!SK || w.kt_end > w.kt_begin) {
+                        iss_mb = w.mb;
+                        iss_nb = w.nb;
+                        iss_kt = w.kt_begin;
+                        iss_kt_end = w.kt_end;
+                        return;
+                    }
                 }
             };
             // lane 0: issue the next k-tile into its ring slot (bounded wait for the slot)
@@ -434,7 +522,7 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
             const int nq = 8 * tg + tt;  // rows 4*nq .. 4*nq + 3 of the B tile
             uint32_t it = 0;
             for (int unit = blockIdx.x; ok && unit < num_units; unit += gridDim.x) {
-                const Unit w = unit_coords(unit, p);
+                const Unit w = unit_coords<SK>(unit, p, sk_cta);
                 for (int kt = w.kt_begin; ok && kt < w.kt_end; ++kt, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
@@ -496,7 +584,7 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
             uint32_t it = 0;
             bool ok = true;
             for (int unit = blockIdx.x; ok && unit < num_units; unit += gridDim.x) {
-                const Unit w = unit_coords(unit, p);
+                const Unit w = unit_coords<SK>(unit, p, sk_cta);
                 const int mb = w.mb, nb = w.nb;
                 for (int kt = w.kt_begin; kt < w.kt_end; ++kt, ++it) {
                     const uint32_t s = it % STAGES;
@@ -555,7 +643,10 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
 
     uint32_t it = 0;
     for (int unit = blockIdx.x; unit < num_units; unit += gridDim.x) {
-        const Unit w = unit_coords(unit, p);
+        const Unit w = unit_coords<SK>(unit, p, sk_cta);
+        if constexpr (SK) {
+            if (w.kt_end <= w.kt_begin) continue;  // an empty stream-K unit: no stages, nothing to write
+        }
         const int mb = w.mb, nb = w.nb;
         // acc2[i][jp] holds columns 2*jp and 2*jp + 1 of row i.
         float2 acc2[8][TN / 2];
@@ -778,10 +869,16 @@ __global__ void __launch_bounds__(256) simt_tail_reduce_kernel(const SimtParams 
         const long long m = (long long)mb * bm + row;
         const int n = nb * bn + col;
         if (m >= p.M || n >= p.N) continue;
-        const float *src = p.partials + (long long)r * tile_elems + e;
+        // the tile's partial tiles in k order: slices s at slot s * tail + r,
+        // or stream-K segments j at slot r * sk_smax + j
+        const bool sk = p.splits == 0;
+        const long long t0 = sk ? (long long)r * p.sk.k_tiles : 0;
+        const int parts = sk ? static_cast<int>(sk_owner(t0 + p.sk.k_tiles - 1, p) - sk_owner(t0, p) + 1) : p.splits;
+        const long long stride = sk ? tile_elems : (long long)p.tail_tiles * tile_elems;
+        const float *src = p.partials + (sk ? (long long)r * p.sk.smax : (long long)r) * tile_elems + e;
         float4 acc = *reinterpret_cast<const float4 *>(src);
-        for (int s = 1; s < p.splits; ++s) {
-            const float4 v = *reinterpret_cast<const float4 *>(src + (long long)s * p.tail_tiles * tile_elems);
+        for (int s = 1; s < parts; ++s) {
+            const float4 v = *reinterpret_cast<const float4 *>(src + s * stride);
             acc.x += v.x;
             acc.y += v.y;
             acc.z += v.z;
@@ -803,6 +900,7 @@ __global__ void __launch_bounds__(256) simt_tail_reduce_kernel(const SimtParams 
 
 struct ConfigEntry {
     int bm, bn_row, bn_col, ctas_per_sm;  // ctas_per_sm 0: not usable on this device
+    bool stream_k;                        // has the stream-K kernels (TMA-loaded operands)
     float rate_row, rate_col;             // measured TFLOP/s in whole waves; 0: not picked automatically
     const char *name;
     cudaError_t (*prepare)(int *ctas_per_sm);
@@ -810,11 +908,11 @@ struct ConfigEntry {
                    int grid, cudaStream_t);
 };
 
-template <int L, int WM, int WN, int TN, int ST, int GU, int F2, int PWG>
+template <int L, int WM, int WN, int TN, int ST, int GU, int F2, int PWG, bool SK>
 cudaError_t prepare_one(int *ctas)
 {
     using S = Simt<L, WM, WN, TN, ST, GU, F2, PWG>;
-    auto k = sgemm_simt_kernel<L, WM, WN, TN, ST, GU, F2, PWG>;
+    auto k = sgemm_simt_kernel<L, WM, WN, TN, ST, GU, F2, PWG, SK>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, k, S::THREADS, S::SMEM_BYTES);
@@ -849,41 +947,63 @@ constexpr int col_stages(int wm, int wn, int tn, int f2, int st)
 // producer warp.
 constexpr int col_pwg(int wn, int tn, int f2, int pwg) { return pwg && col_layout(wn, tn, f2) == 2 ? 1 : 0; }
 
-template <int WM, int WN, int TN, int ST, int GU, int F2, int PWG>
+// SKF: the configuration also has stream-K kernels for TMA-loaded operands
+// (layouts 0, 1 and 2); the element-wise producer (layout 3) always cuts
+// the tail into slices.
+template <int WM, int WN, int TN, int ST, int GU, int F2, int PWG, bool SKF>
 cudaError_t prepare_cfg(int *ctas)
 {
-    int c0 = 0, c1 = 0, c3 = 0;
-    cudaError_t e = prepare_one<0, WM, WN, TN, ST, GU, F2, PWG>(&c0);
-    if (e == cudaSuccess)
-        e = prepare_one<col_layout(WN, TN, F2), WM, WN, col_tn(TN), col_stages(WM, WN, TN, F2, ST), GU, F2,
-                        col_pwg(WN, TN, F2, PWG)>(&c1);
-    if (e == cudaSuccess) e = prepare_one<3, WM, WN, TN, ST, GU, F2, PWG>(&c3);
-    *ctas = c0 < c1 ? c0 : c1;
-    *ctas = *ctas < c3 ? *ctas : c3;
+    constexpr int CL = col_layout(WN, TN, F2), CST = col_stages(WM, WN, TN, F2, ST);
+    constexpr int CT = col_tn(TN), CP = col_pwg(WN, TN, F2, PWG);
+    int c0 = 0, c1 = 0, c3 = 0, s0 = 1, s1 = 1;
+    cudaError_t e = prepare_one<0, WM, WN, TN, ST, GU, F2, PWG, false>(&c0);
+    if (e == cudaSuccess) e = prepare_one<CL, WM, WN, CT, CST, GU, F2, CP, false>(&c1);
+    if (e == cudaSuccess) e = prepare_one<3, WM, WN, TN, ST, GU, F2, PWG, false>(&c3);
+    if constexpr (SKF) {
+        if (e == cudaSuccess) e = prepare_one<0, WM, WN, TN, ST, GU, F2, PWG, true>(&s0);
+        if (e == cudaSuccess) e = prepare_one<CL, WM, WN, CT, CST, GU, F2, CP, true>(&s1);
+    }
+    int c = c0 < c1 ? c0 : c1;
+    c = c < c3 ? c : c3;
+    c = c < s0 ? c : s0;
+    *ctas = c < s1 ? c : s1;
     return e;
 }
 
-template <int WM, int WN, int TN, int ST, int GU, int F2, int PWG>
-void launch_cfg(int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB, const SimtParams &p,
-                int grid, cudaStream_t stream)
+template <int WM, int WN, int TN, int ST, int GU, int F2, int PWG, bool SK>
+void launch_form(int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB, const SimtParams &p,
+                 int grid, cudaStream_t stream)
 {
     if (layout_b == 0) {
         using S = Simt<0, WM, WN, TN, ST, GU, F2, PWG>;
-        sgemm_simt_kernel<0, WM, WN, TN, ST, GU, F2, PWG><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
+        sgemm_simt_kernel<0, WM, WN, TN, ST, GU, F2, PWG, SK><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
     } else if (layout_b == 3) {
         using S = Simt<3, WM, WN, TN, ST, GU, F2, PWG>;
-        sgemm_simt_kernel<3, WM, WN, TN, ST, GU, F2, PWG><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
+        sgemm_simt_kernel<3, WM, WN, TN, ST, GU, F2, PWG, false><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
     } else {
         constexpr int L = col_layout(WN, TN, F2), CST = col_stages(WM, WN, TN, F2, ST);
         constexpr int CP = col_pwg(WN, TN, F2, PWG);
         using S = Simt<L, WM, WN, col_tn(TN), CST, GU, F2, CP>;
-        sgemm_simt_kernel<L, WM, WN, col_tn(TN), CST, GU, F2, CP><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
+        sgemm_simt_kernel<L, WM, WN, col_tn(TN), CST, GU, F2, CP, SK><<<grid, S::THREADS, S::SMEM_BYTES, stream>>>(tmA, tmB, p);
     }
 }
 
-#define DG_SIMT_CFG(WM, WN, TN, ST, GU, F2, PWG, RATE_ROW, RATE_COL, NAME)                           \
-    {WM * 32,  WN * 8 * TN, WN * 8 * col_tn(TN), 0, RATE_ROW, RATE_COL, NAME,                          \
-     prepare_cfg<WM, WN, TN, ST, GU, F2, PWG>, launch_cfg<WM, WN, TN, ST, GU, F2, PWG>}
+template <int WM, int WN, int TN, int ST, int GU, int F2, int PWG, bool SKF>
+void launch_cfg(int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB, const SimtParams &p,
+                int grid, cudaStream_t stream)
+{
+    if constexpr (SKF) {
+        if (p.splits == 0) {
+            launch_form<WM, WN, TN, ST, GU, F2, PWG, true>(layout_b, tmA, tmB, p, grid, stream);
+            return;
+        }
+    }
+    launch_form<WM, WN, TN, ST, GU, F2, PWG, false>(layout_b, tmA, tmB, p, grid, stream);
+}
+
+#define DG_SIMT_CFG(WM, WN, TN, ST, GU, F2, PWG, SKF, RATE_ROW, RATE_COL, NAME)                      \
+    {WM * 32,  WN * 8 * TN, WN * 8 * col_tn(TN), 0, SKF, RATE_ROW, RATE_COL, NAME,                     \
+     prepare_cfg<WM, WN, TN, ST, GU, F2, PWG, SKF>, launch_cfg<WM, WN, TN, ST, GU, F2, PWG, SKF>}
 
 // Config table; GEMM_OPT_SIMT_CONFIG selects entry (value - 1).  Rates are
 // TFLOP/s measured on GB300 at sizes that fill whole waves (M = 7296,
@@ -901,14 +1021,14 @@ void launch_cfg(int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB, co
 // never win; they stay selectable.  With scalar FMAs instead of packed pairs
 // the 192x128 tile is issue-bound (57.7).
 ConfigEntry g_configs[] = {
-    DG_SIMT_CFG(4, 2, 8, 6, 8, 1, 0, 69.0f, 63.5f, "128x128"),
-    DG_SIMT_CFG(4, 2, 8, 6, 8, 0, 0, 0.0f, 0.0f, "128x128s"),
-    DG_SIMT_CFG(2, 2, 8, 4, 8, 1, 0, 58.9f, 51.4f, "64x128"),
-    DG_SIMT_CFG(2, 1, 8, 4, 8, 1, 0, 31.5f, 29.3f, "64x64"),
-    DG_SIMT_CFG(4, 2, 16, 4, 8, 1, 1, 0.0f, 0.0f, "128x256r"),
-    DG_SIMT_CFG(6, 2, 8, 4, 8, 1, 1, 70.3f, 67.1f, "192x128r"),
-    DG_SIMT_CFG(4, 4, 4, 6, 8, 1, 1, 66.6f, 0.0f, "128x128w16"),
-    DG_SIMT_CFG(8, 2, 8, 4, 8, 1, 1, 0.0f, 0.0f, "256x128r"),
+    DG_SIMT_CFG(4, 2, 8, 6, 8, 1, 0, true, 69.0f, 63.5f, "128x128"),
+    DG_SIMT_CFG(4, 2, 8, 6, 8, 0, 0, false, 0.0f, 0.0f, "128x128s"),
+    DG_SIMT_CFG(2, 2, 8, 4, 8, 1, 0, true, 58.9f, 51.4f, "64x128"),
+    DG_SIMT_CFG(2, 1, 8, 4, 8, 1, 0, true, 31.5f, 29.3f, "64x64"),
+    DG_SIMT_CFG(4, 2, 16, 4, 8, 1, 1, false, 0.0f, 0.0f, "128x256r"),
+    DG_SIMT_CFG(6, 2, 8, 4, 8, 1, 1, true, 70.3f, 67.1f, "192x128r"),
+    DG_SIMT_CFG(4, 4, 4, 6, 8, 1, 1, false, 66.6f, 0.0f, "128x128w16"),
+    DG_SIMT_CFG(8, 2, 8, 4, 8, 1, 1, false, 0.0f, 0.0f, "256x128r"),
 };
 constexpr int kNumConfigs = sizeof(g_configs) / sizeof(g_configs[0]);
 
@@ -933,6 +1053,11 @@ cudaError_t prepare_simt()
 
 int simt_num_configs() { return kNumConfigs; }
 
+bool simt_has_stream_k(int config)
+{
+    return config >= 0 && config < kNumConfigs && g_configs[config].stream_k;
+}
+
 bool simt_config_usable(int config)
 {
     return config >= 0 && config < kNumConfigs && g_configs[config].ctas_per_sm > 0;
@@ -946,26 +1071,47 @@ SimtTile simt_tile(int config, int layout_b)
 
 namespace {
 
-// Persistent waves a shape takes on `slots` CTA slots, counting a split
-// partial last wave as the fraction of a wave it lasts.
-double effective_waves(int config, int layout_b, int64_t M, int64_t N, int64_t K, int64_t slots)
+// Estimated time of an M x N x K product on `config` ("GEMM 性能优化",
+// Wave 模型), in units of 2K / 1e12 seconds.  The measured whole-wave rate
+// is with ctas_per_sm CTAs on every SM; a CTA that shares its SM with k - 1
+// others is taken to run at 1/k of the SM's share of that rate, so its tile
+// takes k x tile area x SMs / rate.  Whole rounds of `slots` tiles, then
+// the partial last round: n CTAs, each running its share g of a tile's K
+// (1 without a split; else the longest slice or stream-K range).
+double simt_cost(int config, int layout_b, int64_t M, int64_t N, int64_t K, int sm_count, int64_t slots,
+                 float rate)
 {
     const SimtTile t = simt_tile(config, layout_b);
     const int64_t tiles = ((M + t.bm - 1) / t.bm) * ((N + t.bn - 1) / t.bn);
+    const int64_t sms = sm_count > 0 ? sm_count : 1;
+    const double tile = double(t.bm) * double(t.bn) * double(sms) / double(rate);
+    auto sharing = [&](int64_t n) {  // CTAs per SM when n run at once
+        int64_t k = (n + sms - 1) / sms;
+        k = k < t.ctas_per_sm ? k : t.ctas_per_sm;
+        return double(k > 1 ? k : 1);
+    };
     const SplitK sk = simt_pick_splits(config, layout_b, M, N, K, slots);
-    const int64_t tail = sk.splits > 1 ? sk.tail_tiles : 0;
-    const double last = tail > 0 ? 1.0 / sk.splits : 0.0;
-    return static_cast<double>((tiles - tail + slots - 1) / slots) + last;
+    const int64_t tail = sk.active() ? sk.tail_tiles : 0;
+    const int64_t whole = tiles - tail;
+    double cost = double(whole / slots) * tile * sharing(slots);
+    if (whole % slots) cost += tile * sharing(whole % slots);
+    if (tail > 0) {
+        const int64_t k_tiles = (K + kSimtBK - 1) / kSimtBK;
+        const double g = double(sk.k_per_split / kSimtBK) / double(k_tiles);
+        const int64_t n = sk.stream_k ? sk.sk_parts : tail * sk.splits;
+        cost += g * tile * sharing(n);
+    }
+    return cost;
 }
 
 }  // namespace
 
 int simt_pick_config(int64_t M, int64_t N, int64_t K, int layout_b, int sm_count, int max_ctas)
 {
-    // The configuration with the least estimated time: effective waves x
-    // tile area / measured rate ("GEMM 性能优化", Wave 模型).  A smaller tile
-    // does not shorten a thread's serial chain of multiply-adds, which is
-    // what bounds an under-filled launch; the K split does.
+    // The configuration with the least estimated time (simt_cost).  A
+    // smaller tile does not shorten a thread's serial chain of
+    // multiply-adds, which is what bounds an under-filled launch; the K
+    // split does.
     int best = 0;
     double best_cost = -1.0;
     for (int c = 0; c < kNumConfigs; ++c) {
@@ -973,8 +1119,7 @@ int simt_pick_config(int64_t M, int64_t N, int64_t K, int layout_b, int sm_count
         const float rate = layout_b == 0 ? e.rate_row : e.rate_col;
         if (rate <= 0.0f || e.ctas_per_sm <= 0) continue;
         const int64_t slots = max_ctas > 0 ? max_ctas : int64_t{sm_count} * e.ctas_per_sm;
-        const SimtTile t = simt_tile(c, layout_b);
-        const double cost = effective_waves(c, layout_b, M, N, K, slots) * t.bm * t.bn / rate;
+        const double cost = simt_cost(c, layout_b, M, N, K, sm_count, slots, rate);
         if (best_cost < 0.0 || cost < best_cost) {
             best_cost = cost;
             best = c;
@@ -983,24 +1128,60 @@ int simt_pick_config(int64_t M, int64_t N, int64_t K, int layout_b, int sm_count
     return best;
 }
 
-SplitK simt_pick_splits(int config, int layout_b, int64_t M, int64_t N, int64_t K, int64_t slots)
+SplitK simt_pick_splits(int config, int layout_b, int64_t M, int64_t N, int64_t K, int64_t slots, int stream_k)
 {
     // Wave model ("GEMM 性能优化", Wave 模型): the tiles that do not fill a
     // whole wave (all of them when there are fewer tiles than slots) are cut
-    // into K slices so that tail x slices fills one wave, each slice at least
-    // four 32-element k-tiles long.
+    // along K.  Slices: tail x slices fills one wave, each slice at least
+    // four 32-element k-tiles long, so the last wave lasts 1/slices of a
+    // wave.  Stream-K: the tail's k-tiles, tile after tile, are shared out
+    // in equal contiguous ranges (at least four k-tiles each) over up to
+    // `slots` CTAs, crossing tile boundaries, so the last wave lasts the
+    // longest range over k-tiles.  Stream-K is taken when it is shorter by
+    // 2 % of a wave or more (1024^3 as 128x128 tiles: 14/32 against 16/32).
     const SimtTile t = simt_tile(config, layout_b);
     const int64_t tiles = ((M + t.bm - 1) / t.bm) * ((N + t.bn - 1) / t.bn);
     const int64_t k_tiles = (K + kSimtBK - 1) / kSimtBK;
     SplitK sk;
-    if (tiles <= 0 || slots <= 0) return sk;
+    if (tiles <= 0 || slots <= 0 || k_tiles <= 0) return sk;
     const int64_t tail = tiles < slots ? tiles : tiles % slots;
     if (tail == 0) return sk;
     int64_t s = slots / tail;
     s = s < k_tiles / 4 ? s : k_tiles / 4;
     s = s < 16 ? s : 16;
-    if (s <= 1) return sk;
-    return simt_split_k(tiles, tail, s, K);
+    const SplitK sliced = s > 1 ? simt_split_k(tiles, tail, s, K) : SplitK();
+    if (stream_k == 1 || !simt_has_stream_k(config)) return sliced;
+    const SplitK streamed = simt_stream_k(tiles, tail, slots, K);
+    if (stream_k == 2) return streamed;
+    const double f_slices = sliced.active() ? double(sliced.k_per_split / kSimtBK) / double(k_tiles) : 1.0;
+    const double f_stream = streamed.active() ? double(streamed.k_per_split / kSimtBK) / double(k_tiles) : 1.0;
+    return f_stream < f_slices - 0.02 ? streamed : sliced;
+}
+
+SplitK simt_stream_k(int64_t tiles, int64_t tail, int64_t ctas, int64_t K)
+{
+    SplitK sk;
+    const int64_t k_tiles = (K + kSimtBK - 1) / kSimtBK;
+    if (tail <= 0 || tail > tiles || ctas <= 0 || k_tiles <= 0) return sk;
+    const int64_t iters = tail * k_tiles;
+    // ranges of at least four k-tiles, as for slices (shorter ones cost more
+    // in partial tiles and fills than they save)
+    const int64_t most = iters / 4 > 1 ? iters / 4 : 1;
+    const int64_t parts = ctas < most ? ctas : most;
+    const int64_t per = (iters + parts - 1) / parts;  // longest range of one CTA
+    sk.stream_k = 1;
+    sk.tail_tiles = tail;
+    sk.sk_ctas = ctas;
+    sk.sk_parts = parts;
+    // every range is at least floor(iters / parts) >= 1 iterations long, so
+    // the ranges meeting one tile's k_tiles iterations number at most
+    // ceil(k_tiles / floor(iters / parts)) + 1
+    const int64_t min_len = iters / parts;
+    sk.sk_smax = (k_tiles + min_len - 1) / min_len + 1;
+    if (sk.sk_smax > parts) sk.sk_smax = parts;
+    sk.splits = 1;
+    sk.k_per_split = static_cast<int>(per * kSimtBK);
+    return sk;
 }
 
 SplitK simt_split_k(int64_t tiles, int64_t tail, int64_t want, int64_t K)
@@ -1024,28 +1205,38 @@ SimtParams simt_params(int config, int layout_b, int M, int N, int K, float *C, 
 {
     const SimtTile t = simt_tile(config, layout_b);
     SimtParams p;
+    memset(&p, 0, sizeof p);
     p.M = M;
     p.N = N;
     p.K = K;
     p.tiles_m = (M + t.bm - 1) / t.bm;
     p.tiles_n = (N + t.bn - 1) / t.bn;
     p.group_m = lc.group_m > 0 ? lc.group_m : 8;
-    const bool split = sk.splits > 1 && sk.tail_tiles > 0;
+    const bool split = sk.active();
+    const bool streamed = split && sk.stream_k;
     p.tail_tiles = split ? static_cast<int>(sk.tail_tiles) : 0;
-    p.splits = split ? sk.splits : 1;
+    p.splits = streamed ? 0 : split ? sk.splits : 1;
     p.k_per_split = split ? sk.k_per_split : K;
     p.full_units = p.tiles_m * p.tiles_n - p.tail_tiles;
     p.partials = split ? sk.partials : nullptr;
+    if (streamed) {
+        p.sk.k_tiles = (K + kSimtBK - 1) / kSimtBK;
+        p.sk.ctas = static_cast<int>(sk.sk_ctas);
+        p.sk.parts = static_cast<int>(sk.sk_parts);
+        p.sk.smax = static_cast<int>(sk.sk_smax);
+        p.sk.iters = (long long)p.tail_tiles * p.sk.k_tiles;
+        // units of the whole tiles, rounded up to whole rounds of the grid,
+        // then each CTA's segments: a range of at most ceil(I / P) iterations
+        // spans at most ceil(ceil(I / P) / k_tiles) + 1 tiles
+        p.sk.base = (p.full_units + p.sk.ctas - 1) / p.sk.ctas * p.sk.ctas;
+        p.sk.kmax = static_cast<int>(((p.sk.iters + p.sk.parts - 1) / p.sk.parts + p.sk.k_tiles - 1) / p.sk.k_tiles + 1);
+    }
     p.C = C;
     p.ldc = ldc;
     p.status = lc.status;
     p.timeout_ns = lc.timeout_ns;
     p.c_vec4 = c_vec4 ? 1 : 0;
     p.debug_drop = lc.debug_drop;
-    p.A = nullptr;
-    p.B = nullptr;
-    p.lda = 0;
-    p.ldb = 0;
     return p;
 }
 
@@ -1055,14 +1246,17 @@ int64_t simt_units(int config, int layout_b, int64_t M, int64_t N, const SplitK 
 {
     const SimtTile t = simt_tile(config, layout_b);
     const int64_t tiles = ((M + t.bm - 1) / t.bm) * ((N + t.bn - 1) / t.bn);
-    return sk.splits > 1 && sk.tail_tiles > 0 ? tiles - sk.tail_tiles + sk.tail_tiles * sk.splits : tiles;
+    if (!sk.active()) return tiles;
+    if (!sk.stream_k) return tiles - sk.tail_tiles + sk.tail_tiles * sk.splits;
+    // The launch grid must be sk_ctas CTAs, each running its whole tiles and
+    // then its segments (the kernel counts those itself); this is the grid.
+    return sk.sk_ctas;
 }
 
 size_t simt_partial_bytes(int config, int layout_b, const SplitK &sk)
 {
     const SimtTile t = simt_tile(config, layout_b);
-    if (sk.splits <= 1 || sk.tail_tiles <= 0) return 0;
-    return static_cast<size_t>(sk.splits) * static_cast<size_t>(sk.tail_tiles) * t.bm * t.bn * sizeof(float);
+    return static_cast<size_t>(sk.partial_tiles()) * t.bm * t.bn * sizeof(float);
 }
 
 cudaError_t launch_simt_f32(int config, const CUtensorMap &tmA, const CUtensorMap &tmB,
@@ -1078,11 +1272,12 @@ cudaError_t launch_simt_f32_elementwise(int config, const float *A, int64_t lda,
                                         int N, int K, float *C, int64_t ldc, bool c_vec4, const LaunchCommon &lc,
                                         const SplitK &sk)
 {
+    if (sk.active() && sk.stream_k) return cudaErrorInvalidValue;  // the element-wise form has no stream-K
     SimtParams p = simt_params(config, 0, M, N, K, C, ldc, c_vec4, lc, sk);
-    p.A = A;
-    p.B = B;
-    p.lda = lda;
-    p.ldb = ldb;
+    p.ew.A = A;
+    p.ew.B = B;
+    p.ew.lda = lda;
+    p.ew.ldb = ldb;
     CUtensorMap unused;
     memset(&unused, 0, sizeof unused);
     g_configs[config].launch(3, unused, unused, p, lc.grid, lc.stream);

@@ -131,6 +131,16 @@ extern "C" {
  * MMA instruction); 0 (default) = the library's choice, at present six
  * stages of one slice (faster on every shape measured).  Same results. */
 #define GEMM_OPT_TC_STAGE_SLICES 13
+/* FP32: how the tiles of a partial last wave share the CTAs, when
+ * GEMM_OPT_SPLIT_K is 0.  0 (default) = whichever of the two the wave model
+ * rates shorter; 1 = K slices of equal length per tile; 2 = stream-K: the
+ * tail tiles' 32-wide k steps, tile after tile, cut into one contiguous range
+ * per CTA (at least four steps each), crossing tile boundaries (a second
+ * kernel adds each tile's pieces in k order).  Same results up to the order
+ * of the additions.  Configurations without stream-K kernels
+ * (GEMM_OPT_SIMT_CONFIG 2, 5, 7, 8) and the element-wise producer
+ * (GEMM_OPT_ELEMENTWISE) always take slices. */
+#define GEMM_OPT_STREAM_K 14
 
 typedef struct gemm_ctx *gemm_handle_t;
 

@@ -134,7 +134,8 @@ def test_unaligned_leading_dimensions(g, oracle_mod, mode, layout):
     """Odd leading dimensions and an offset base pointer, which TMA cannot
     address: re-packed first; FP32 with row-major B can instead copy them
     element by element into the shared-memory ring (cp.async,
-    GEMM_OPT_ELEMENTWISE = 1).  Same bits either way."""
+    GEMM_OPT_ELEMENTWISE = 1).  Same bits either way, given the same K split
+    (the element-wise form has no stream-K, so both runs take slices)."""
     from dense_gemm_sm100_gb300 import gemm
     M, N, K = 97, 203, 151
     A, B = inp.make_operands(M, N, K, layout_b=layout, seed=23, dist="normal", dtype=mode)
@@ -146,19 +147,23 @@ def test_unaligned_leading_dimensions(g, oracle_mod, mode, layout):
     Bp[:, 1:cols_b + 1] = B.to(dev)
     Cbig = torch.zeros((M, N + 1), dtype=torch.float32, device=dev)
     C = Cbig[:, :N]
-    g.run(Ap[:, 1:K + 1], Bp[:, 1:cols_b + 1], C, layout, mode)
-    g.sync_status()
-    assert "repackA" in g.last_path and "repackB" in g.last_path
-    if mode == "f32" and layout == ROW:
-        C_first = C.clone()
-        g.set_option(gemm.GEMM_OPT_ELEMENTWISE, 1)
-        try:
-            g.run(Ap[:, 1:K + 1], Bp[:, 1:cols_b + 1], C, layout, mode)
-            g.sync_status()
-            assert "+cpasync" in g.last_path and "repack" not in g.last_path, g.last_path
-        finally:
-            g.set_option(gemm.GEMM_OPT_ELEMENTWISE, 0)
-        assert torch.equal(C_first, C)
+    g.set_option(gemm.GEMM_OPT_STREAM_K, 1)
+    try:
+        g.run(Ap[:, 1:K + 1], Bp[:, 1:cols_b + 1], C, layout, mode)
+        g.sync_status()
+        assert "repackA" in g.last_path and "repackB" in g.last_path
+        if mode == "f32" and layout == ROW:
+            C_first = C.clone()
+            g.set_option(gemm.GEMM_OPT_ELEMENTWISE, 1)
+            try:
+                g.run(Ap[:, 1:K + 1], Bp[:, 1:cols_b + 1], C, layout, mode)
+                g.sync_status()
+                assert "+cpasync" in g.last_path and "repack" not in g.last_path, g.last_path
+            finally:
+                g.set_option(gemm.GEMM_OPT_ELEMENTWISE, 0)
+            assert torch.equal(C_first, C)
+    finally:
+        g.set_option(gemm.GEMM_OPT_STREAM_K, 0)
     Cr, S = oracle_of(oracle_mod, A, B, layout)
     assert_parity(C, Cr, S, TOL[mode])
 
@@ -565,37 +570,91 @@ def test_split_k_integer_exact(g, oracle_mod):
 
 
 def test_split_k_chosen_for_underfilled_shape(g):
-    """1024^3 fills 64 of the SMs with 128x128 tiles: split-K is chosen."""
+    """1024^3 fills 64 of the SMs with 128x128 tiles: the K dimension is
+    split, as stream-K (32 k-tiles of 64 tiles on 152 CTAs, 14 each) since
+    that is shorter than two slices of 16."""
     A, B = inp.make_operands(1024, 1024, 1024, layout_b=COL, seed=1)
     run_gpu(g, A, B, COL, "f32")
-    assert "splitk" in g.last_path
+    assert "+splitk" in g.last_path or "+streamk" in g.last_path, g.last_path
 
 
+@pytest.mark.parametrize("stream_k", [1, 2])
 @pytest.mark.parametrize("config,layout,M", [(1, ROW, 700), (1, COL, 700), (6, ROW, 500)])
-def test_tail_tiles_split_along_k(g, oracle_mod, config, layout, M):
-    """Tiles of a partial last wave are cut into K slices spread over all CTA
-    slots, and a second kernel adds the slices in order ("GEMM 性能优化",
-    Wave 模型).  An 8-CTA cap makes the wave small: 700 rows x 650 columns
-    in 128x128 tiles is 36 tiles = 4 waves + 4 tiles, 500 rows in 192x128
-    tiles is 18 tiles = 2 waves + 2 tiles.  Same tolerance, deterministic,
-    and exact on integer inputs."""
+def test_tail_tiles_split_along_k(g, oracle_mod, config, layout, M, stream_k):
+    """Tiles of a partial last wave are cut along K and spread over all CTA
+    slots, and a second kernel adds each tile's pieces in k order ("GEMM
+    性能优化", Wave 模型): as equal slices per tile (stream_k 1) or as one
+    equal, contiguous range of the tail's k-tiles per CTA that may cross
+    tile boundaries (stream-K, 2).  An 8-CTA cap makes the wave small: 700
+    rows x 650 columns in 128x128 tiles is 36 tiles = 4 waves + 4 tiles,
+    500 rows in 192x128 tiles is 18 tiles = 2 waves + 2 tiles.  Same
+    tolerance, deterministic, and exact on integer inputs."""
     from dense_gemm_sm100_gb300 import gemm
     N, K = 650, 640
     g.set_option(gemm.GEMM_OPT_MAX_CTAS, 8)
     g.set_option(gemm.GEMM_OPT_SIMT_CONFIG, config)
+    g.set_option(gemm.GEMM_OPT_STREAM_K, stream_k)
     try:
         A, B = inp.make_operands(M, N, K, layout_b=layout, dist="normal", seed=M + config)
         C1 = run_gpu(g, A, B, layout, "f32").cpu()
-        assert "+tail" in g.last_path, g.last_path
+        assert ("+tail" if stream_k == 1 else "+streamk") in g.last_path, g.last_path
         C2 = run_gpu(g, A, B, layout, "f32").cpu()
         Ai, Bi = inp.make_integer_operands(M, N, K, layout_b=layout, seed=config)
         Ci = run_gpu(g, Ai, Bi, layout, "f32")
     finally:
         g.set_option(gemm.GEMM_OPT_MAX_CTAS, 0)
         g.set_option(gemm.GEMM_OPT_SIMT_CONFIG, 0)
+        g.set_option(gemm.GEMM_OPT_STREAM_K, 0)
     assert torch.equal(C1, C2)
     Cr, S = oracle_of(oracle_mod, A, B, layout)
-    assert_parity(C1, Cr, S, TOL["f32"], f"tail split config {config}")
+    assert_parity(C1, Cr, S, TOL["f32"], f"tail split config {config} stream_k {stream_k}")
+    Cri, _ = oracle_of(oracle_mod, Ai, Bi, layout)
+    assert np.array_equal(to_f64(Ci), Cri)
+
+
+@pytest.mark.parametrize("config,layout,shape,max_ctas,elementwise", [
+    (1, COL, (1024, 1024, 1024), 0, 0),  # 64 tiles, 2048 k-tiles on 152 CTAs: ranges cross tiles
+    (6, COL, (1000, 900, 1000), 0, 0),   # 192x128, corner turn, ragged M, N and K
+    (1, ROW, (700, 651, 640), 8, 0),     # N not a multiple of 4: element-wise C writes
+    (1, ROW, (300, 520, 40), 8, 0),      # 2 k-tiles per tile: ranges of two tiles' pieces
+    (1, ROW, (130, 130, 64), 0, 0),      # 8 k-tiles in all, fewer than the CTAs: most CTAs idle
+    (4, ROW, (200, 300, 700), 16, 0),    # 64x64 tiles
+    (6, ROW, (1000, 1000, 3000), 0, 0),  # 192x128, 48 tiles x 94 k-tiles: several pieces per tile
+    (1, ROW, (333, 444, 555), 8, 1),     # element-wise producer: no stream-K form, slices instead
+])
+def test_stream_k_forced(g, oracle_mod, config, layout, shape, max_ctas, elementwise):
+    """Stream-K forced on shapes whose tiles all fit in one wave: every CTA
+    takes an equal range of the k-tiles, tile after tile, writes one partial
+    tile per tile its range touches, and a second kernel adds each tile's
+    partial tiles in k order.  Same tolerance, deterministic, exact on
+    integer inputs.  The element-wise producer has no stream-K form and cuts
+    the tiles into slices."""
+    from dense_gemm_sm100_gb300 import gemm
+    M, N, K = shape
+    g.set_option(gemm.GEMM_OPT_SIMT_CONFIG, config)
+    g.set_option(gemm.GEMM_OPT_STREAM_K, 2)
+    g.set_option(gemm.GEMM_OPT_MAX_CTAS, max_ctas)
+    g.set_option(gemm.GEMM_OPT_ELEMENTWISE, elementwise)
+    try:
+        # K = 555: A's pitch of 2220 bytes is no multiple of 16, so TMA cannot
+        # address A and the element-wise case copies it with cp.async
+        A, B = inp.make_operands(M, N, K, layout_b=layout, dist="normal", seed=M + N + K)
+        C1 = run_gpu(g, A, B, layout, "f32").cpu()
+        if elementwise:
+            assert "+cpasync" in g.last_path and "+tail" in g.last_path, g.last_path
+        else:
+            assert "+streamk" in g.last_path, g.last_path
+        C2 = run_gpu(g, A, B, layout, "f32").cpu()
+        Ai, Bi = inp.make_integer_operands(M, N, K, layout_b=layout, seed=K)
+        Ci = run_gpu(g, Ai, Bi, layout, "f32")
+    finally:
+        g.set_option(gemm.GEMM_OPT_SIMT_CONFIG, 0)
+        g.set_option(gemm.GEMM_OPT_STREAM_K, 0)
+        g.set_option(gemm.GEMM_OPT_MAX_CTAS, 0)
+        g.set_option(gemm.GEMM_OPT_ELEMENTWISE, 0)
+    assert torch.equal(C1, C2)
+    Cr, S = oracle_of(oracle_mod, A, B, layout)
+    assert_parity(C1, Cr, S, TOL["f32"], f"stream-K {shape} config {config}")
     Cri, _ = oracle_of(oracle_mod, Ai, Bi, layout)
     assert np.array_equal(to_f64(Ci), Cri)
 

@@ -1,8 +1,8 @@
 """Seeded random shapes across every path the dispatcher can take: all three
 modes, both B layouts, the FP32 tile configurations (128x128 with 8 or 16
 consumer warps, 192x128), the tensor-core CTA modes, and CTA caps that make
-the tail split and the tensor-core K split run on small problems, on device
-or host buffers.  Each result is checked
+the tail split (as slices or stream-K) and the tensor-core K split run on
+small problems, on device or host buffers.  Each result is checked
 against the oracle within the mode's tolerance; integer inputs must match
 exactly."""
 import random
@@ -34,7 +34,11 @@ def cases():
         integer = rng.random() < 0.3
         elementwise = 1 if (mode == "f32" and layout == inp.B_ROW_MAJOR and rng.random() < 0.3) else 0
         host = rng.random() < 0.2  # through gemm_run_host (pinned host buffers)
-        out.append((i, mode, layout, (M, N, K), simt_config, tc_mode, max_ctas, integer, host, elementwise))
+        # FP32 tail split: chosen, slices or stream-K (own generator, so the
+        # cases above stay as they were)
+        stream_k = random.Random(1000 + i).choice([0, 0, 1, 2])
+        out.append((i, mode, layout, (M, N, K), simt_config, tc_mode, max_ctas, integer, host, elementwise,
+                    stream_k))
     return out
 
 
@@ -52,7 +56,7 @@ def g():
 @pytest.mark.parametrize("case", cases(), ids=lambda c: f"case{c[0]}")
 def test_random_shape(g, oracle_mod, case):
     from dense_gemm_sm100_gb300 import gemm
-    _, mode, layout, (M, N, K), simt_config, tc_mode, max_ctas, integer, host, elementwise = case
+    _, mode, layout, (M, N, K), simt_config, tc_mode, max_ctas, integer, host, elementwise, stream_k = case
     if integer:
         A, B = inp.make_integer_operands(M, N, K, layout_b=layout, seed=M * 7 + N, dtype=mode)
     else:
@@ -61,6 +65,7 @@ def test_random_shape(g, oracle_mod, case):
     g.set_option(gemm.GEMM_OPT_TC_CLUSTER, tc_mode)
     g.set_option(gemm.GEMM_OPT_MAX_CTAS, max_ctas)
     g.set_option(gemm.GEMM_OPT_ELEMENTWISE, elementwise)
+    g.set_option(gemm.GEMM_OPT_STREAM_K, stream_k)
     try:
         if host:
             C = torch.full((M, N), float("nan")).pin_memory()
@@ -77,6 +82,7 @@ def test_random_shape(g, oracle_mod, case):
         g.set_option(gemm.GEMM_OPT_TC_CLUSTER, 3)
         g.set_option(gemm.GEMM_OPT_MAX_CTAS, 0)
         g.set_option(gemm.GEMM_OPT_ELEMENTWISE, 0)
+        g.set_option(gemm.GEMM_OPT_STREAM_K, 0)
     Cr, S = oracle_mod.gemm(to_f64(A), to_f64(B), layout)
     if integer:
         assert np.array_equal(to_f64(C), Cr), path
