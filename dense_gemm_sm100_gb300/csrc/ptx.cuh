@@ -31,6 +31,24 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
+// ------------------------------------------- programmatic dependent launch
+
+// Lets the kernel launched after this one on the stream with programmatic
+// stream serialisation be scheduled before this grid ends (its CTAs start
+// once resources free up and wait in griddep_wait).
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the grids this one depends on have completed and their memory
+// operations are visible; a no-op for a kernel launched without the
+// programmatic serialisation attribute.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)

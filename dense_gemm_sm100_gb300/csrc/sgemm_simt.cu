@@ -305,6 +305,9 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
         fence_barrier_init();
     }
     __syncthreads();
+    // the tail reduction, if one follows, may be scheduled now; it waits for
+    // this grid to end before it reads anything
+    griddep_launch_dependents();
 
     // Every producer role sits inside this one branch, after the register
     // release: ptxas then budgets the consumer code below with the consumers'
@@ -851,31 +854,44 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
     }
 }
 
-// C for the tail tiles: the sum of their K-slice partial tiles, added in
-// slice order s = 0, 1, ... (deterministic; exact for integer data).  One
-// thread per 4 consecutive columns of a tile row.
+// C for the tail tiles: the sum of their partial tiles, added in k order
+// (slice s = 0, 1, ... or stream-K segment j = 0, 1, ...; deterministic,
+// exact for integer data).  Block (r, c) covers tail tile r, chunk c of its
+// rows of 4-column groups, so the tile's coordinates and pieces are worked
+// out once per thread, not per group.  Launched as a programmatic dependent
+// of the GEMM kernel: it may start before the GEMM ends and waits for it in
+// griddep_wait.
 __global__ void __launch_bounds__(256) simt_tail_reduce_kernel(const SimtParams p, int bm, int bn)
 {
-    const int quads = bm * bn / 4;
-    const long long total = (long long)p.tail_tiles * quads;
+    griddep_wait();
+    const int r = blockIdx.x;
+    int mb, nb;
+    tile_coords(p.full_units + r, p, mb, nb);
     const long long tile_elems = (long long)bm * bn;
-    for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < total;
-         q += (long long)gridDim.x * blockDim.x) {
-        const int r = static_cast<int>(q / quads);
-        const int e = static_cast<int>(q - (long long)r * quads) * 4;
-        const int row = e / bn, col = e - (e / bn) * bn;
-        int mb, nb;
-        tile_coords(p.full_units + r, p, mb, nb);
-        const long long m = (long long)mb * bm + row;
-        const int n = nb * bn + col;
+    const bool sk = p.splits == 0;
+    int parts;
+    long long stride;
+    const float *base;
+    if (sk) {  // segments j at slot r * smax + j
+        const long long t0 = (long long)r * p.sk.k_tiles;
+        parts = static_cast<int>(sk_owner(t0 + p.sk.k_tiles - 1, p) - sk_owner(t0, p) + 1);
+        stride = tile_elems;
+        base = p.partials + (long long)r * p.sk.smax * tile_elems;
+    } else {  // slices s at slot s * tail + r
+        parts = p.splits;
+        stride = (long long)p.tail_tiles * tile_elems;
+        base = p.partials + (long long)r * tile_elems;
+    }
+    const long long m_tile = (long long)mb * bm;
+    const int n_tile = nb * bn;
+    const int quads = bm * bn / 4;
+    for (int q = blockIdx.y * blockDim.x + threadIdx.x; q < quads; q += gridDim.y * blockDim.x) {
+        const int e = q * 4;
+        const int row = e / bn, col = e - row * bn;
+        const long long m = m_tile + row;
+        const int n = n_tile + col;
         if (m >= p.M || n >= p.N) continue;
-        // the tile's partial tiles in k order: slices s at slot s * tail + r,
-        // or stream-K segments j at slot r * sk_smax + j
-        const bool sk = p.splits == 0;
-        const long long t0 = sk ? (long long)r * p.sk.k_tiles : 0;
-        const int parts = sk ? static_cast<int>(sk_owner(t0 + p.sk.k_tiles - 1, p) - sk_owner(t0, p) + 1) : p.splits;
-        const long long stride = sk ? tile_elems : (long long)p.tail_tiles * tile_elems;
-        const float *src = p.partials + (sk ? (long long)r * p.sk.smax : (long long)r) * tile_elems + e;
+        const float *src = base + e;
         float4 acc = *reinterpret_cast<const float4 *>(src);
         for (int s = 1; s < parts; ++s) {
             const float4 v = *reinterpret_cast<const float4 *>(src + s * stride);
@@ -1137,8 +1153,10 @@ SplitK simt_pick_splits(int config, int layout_b, int64_t M, int64_t N, int64_t 
     // wave.  Stream-K: the tail's k-tiles, tile after tile, are shared out
     // in equal contiguous ranges (at least four k-tiles each) over up to
     // `slots` CTAs, crossing tile boundaries, so the last wave lasts the
-    // longest range over k-tiles.  Stream-K is taken when it is shorter by
-    // 2 % of a wave or more (1024^3 as 128x128 tiles: 14/32 against 16/32).
+    // longest range over k-tiles.  Stream-K is taken when that is shorter
+    // (1024^3 as 128x128 tiles: 14/32 against 16/32 of a wave; 8192^3 as
+    // 192x128 tiles: 27/256 against 29/256, measured 0.5 % faster); on a tie,
+    // slices.
     const SimtTile t = simt_tile(config, layout_b);
     const int64_t tiles = ((M + t.bm - 1) / t.bm) * ((N + t.bn - 1) / t.bn);
     const int64_t k_tiles = (K + kSimtBK - 1) / kSimtBK;
@@ -1155,7 +1173,7 @@ SplitK simt_pick_splits(int config, int layout_b, int64_t M, int64_t N, int64_t 
     if (stream_k == 2) return streamed;
     const double f_slices = sliced.active() ? double(sliced.k_per_split / kSimtBK) / double(k_tiles) : 1.0;
     const double f_stream = streamed.active() ? double(streamed.k_per_split / kSimtBK) / double(k_tiles) : 1.0;
-    return f_stream < f_slices - 0.02 ? streamed : sliced;
+    return f_stream < f_slices ? streamed : sliced;
 }
 
 SplitK simt_stream_k(int64_t tiles, int64_t tail, int64_t ctas, int64_t K)
@@ -1290,12 +1308,22 @@ cudaError_t launch_simt_tail_reduce(int config, int layout_b, int M, int N, int 
     const SimtParams p = simt_params(config, layout_b, M, N, K, C, ldc, c_vec4, lc, sk);
     if (p.tail_tiles == 0) return cudaSuccess;
     const SimtTile t = simt_tile(config, layout_b);
-    const long long threads = (long long)p.tail_tiles * (t.bm * t.bn / 4);
-    long long blocks = (threads + 255) / 256;
-    const long long cap = 8LL * (sm_count > 0 ? sm_count : 1);
-    if (blocks > cap) blocks = cap;
-    simt_tail_reduce_kernel<<<static_cast<int>(blocks), 256, 0, lc.stream>>>(p, t.bm, t.bn);
-    return cudaGetLastError();
+    // about four blocks of 256 threads per SM in all, at most one per 256
+    // groups of 4 columns of a tile
+    const int quads = t.bm * t.bn / 4;
+    const long long want = (4LL * (sm_count > 0 ? sm_count : 1) + p.tail_tiles - 1) / p.tail_tiles;
+    const int chunks = static_cast<int>(want < 1 ? 1 : want > quads / 256 ? quads / 256 : want);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.tail_tiles), static_cast<unsigned>(chunks > 0 ? chunks : 1), 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = lc.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, simt_tail_reduce_kernel, p, t.bm, t.bn);
 }
 
 }  // namespace dg
