@@ -60,12 +60,12 @@ NOMINAL_PF = {"bf16": 2.25, "tf32": 1.1, "f32x3": 1.1 / 3}  # f32x3: three TF32 
 # captured for this version of the kernel.
 # Key: workload name -> (bytes per launch, summary file under profiles/).
 NCU_TRAFFIC: dict[str, tuple[float, str]] = {
-    "fp32_8192_row": (None, "profiles/dram_traffic_per_kernel.md: to be re-captured (stream-K kernel)"),
-    "fp32_4095x3073x2047_row": (None, "profiles/dram_traffic_per_kernel.md: to be re-captured (stream-K kernel)"),
-    "ffn_bf16_8192x14336x4096": (498.0e6 + 439.8e6, "profiles/dram_traffic_per_kernel.md"),
-    "ffn_tf32_8192x14336x4096": (2370.8e6 + 455.2e6, "profiles/dram_traffic_per_kernel.md"),
+    "fp32_8192_row": (2836.4e6 + 267.4e6, "profiles/dram_traffic_per_kernel.md"),
+    "fp32_4095x3073x2047_row": (61.0e6 + 22.1e6, "profiles/dram_traffic_per_kernel.md"),
+    "ffn_bf16_8192x14336x4096": (467.1e6 + 435.8e6, "profiles/dram_traffic_per_kernel.md"),
+    "ffn_tf32_8192x14336x4096": (1806.8e6 + 448.1e6, "profiles/dram_traffic_per_kernel.md"),
     # the dominant kernel of the mode: the TF32 product over 3K
-    "fp32x3_8192_row": (16186.3e6 + 265.3e6, "profiles/dram_traffic_per_kernel.md"),
+    "fp32x3_8192_row": (10363.2e6 + 262.5e6, "profiles/dram_traffic_per_kernel.md"),
 }
 
 DESCRIPTIONS = {
