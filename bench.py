@@ -504,6 +504,8 @@ def apply_options(g, args):
         g.set_option(gemm.GEMM_OPT_SPLIT_K, args.split_k)
     if args.tc_group_m:
         g.set_option(gemm.GEMM_OPT_TC_GROUP_M, args.tc_group_m)
+    if args.simt_group_m:
+        g.set_option(gemm.GEMM_OPT_SIMT_GROUP_M, args.simt_group_m)
 
 
 def run_configs(args):
@@ -704,6 +706,8 @@ def main(argv=None):
                     help="force the tensor-core mode (GEMM_OPT_TC_CLUSTER: 1 one CTA per tile, 3 pair MMA; 0 = default)")
     ap.add_argument("--tc-group-m", type=int, default=0,
                     help="GEMM_OPT_TC_GROUP_M: tensor-core tile-order group height in units (0 = chosen)")
+    ap.add_argument("--simt-group-m", type=int, default=0,
+                    help="GEMM_OPT_SIMT_GROUP_M: FP32 SIMT tile-order group height in tile rows (0 = chosen)")
     ap.add_argument("--split-k", type=int, default=0,
                     help="GEMM_OPT_SPLIT_K (0 = chosen per shape, 1 = never, n = n slices)")
     ap.add_argument("--results", default=None,
