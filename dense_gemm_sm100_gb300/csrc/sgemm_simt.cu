@@ -857,33 +857,39 @@ __global__ void __launch_bounds__(Simt<LAYOUT_B, WM, WN, TN, STAGES, GU, F2, PWG
 // C for the tail tiles: the sum of their partial tiles, added in k order
 // (slice s = 0, 1, ... or stream-K segment j = 0, 1, ...; deterministic,
 // exact for integer data).  Block (r, c) covers tail tile r, chunk c of its
-// rows of 4-column groups, so the tile's coordinates and pieces are worked
-// out once per thread, not per group.  Launched as a programmatic dependent
-// of the GEMM kernel: it may start before the GEMM ends and waits for it in
-// griddep_wait.
+// groups of 4 columns, one group per thread where the grid allows; thread 0
+// works out the tile's coordinates and pieces once for the block.  A
+// thread issues the loads of up to 8 pieces before it adds them (in order),
+// so they wait out one L2 round trip together, not one each.  Launched as
+// a programmatic dependent of the GEMM kernel: it may start before the GEMM
+// ends and waits for it in griddep_wait.
 __global__ void __launch_bounds__(256) simt_tail_reduce_kernel(const SimtParams p, int bm, int bn)
 {
-    griddep_wait();
+    __shared__ long long s_m_tile, s_base, s_stride;
+    __shared__ int s_n_tile, s_parts;
     const int r = blockIdx.x;
-    int mb, nb;
-    tile_coords(p.full_units + r, p, mb, nb);
-    const long long tile_elems = (long long)bm * bn;
-    const bool sk = p.splits == 0;
-    int parts;
-    long long stride;
-    const float *base;
-    if (sk) {  // segments j at slot r * smax + j
-        const long long t0 = (long long)r * p.sk.k_tiles;
-        parts = static_cast<int>(sk_owner(t0 + p.sk.k_tiles - 1, p) - sk_owner(t0, p) + 1);
-        stride = tile_elems;
-        base = p.partials + (long long)r * p.sk.smax * tile_elems;
-    } else {  // slices s at slot s * tail + r
-        parts = p.splits;
-        stride = (long long)p.tail_tiles * tile_elems;
-        base = p.partials + (long long)r * tile_elems;
+    if (threadIdx.x == 0) {
+        int mb, nb;
+        tile_coords(p.full_units + r, p, mb, nb);
+        const long long tile_elems = (long long)bm * bn;
+        if (p.splits == 0) {  // stream-K segments j at slot r * smax + j
+            const long long t0 = (long long)r * p.sk.k_tiles;
+            s_parts = static_cast<int>(sk_owner(t0 + p.sk.k_tiles - 1, p) - sk_owner(t0, p) + 1);
+            s_stride = tile_elems;
+            s_base = (long long)r * p.sk.smax * tile_elems;
+        } else {  // slices s at slot s * tail + r
+            s_parts = p.splits;
+            s_stride = (long long)p.tail_tiles * tile_elems;
+            s_base = (long long)r * tile_elems;
+        }
+        s_m_tile = (long long)mb * bm;
+        s_n_tile = nb * bn;
     }
-    const long long m_tile = (long long)mb * bm;
-    const int n_tile = nb * bn;
+    __syncthreads();
+    const long long m_tile = s_m_tile, stride = s_stride;
+    const int n_tile = s_n_tile, parts = s_parts;
+    griddep_wait();  // the partial tiles are complete and visible from here on
+    const float *base = p.partials + s_base;
     const int quads = bm * bn / 4;
     for (int q = blockIdx.y * blockDim.x + threadIdx.x; q < quads; q += gridDim.y * blockDim.x) {
         const int e = q * 4;
@@ -892,13 +898,26 @@ __global__ void __launch_bounds__(256) simt_tail_reduce_kernel(const SimtParams 
         const int n = n_tile + col;
         if (m >= p.M || n >= p.N) continue;
         const float *src = base + e;
-        float4 acc = *reinterpret_cast<const float4 *>(src);
-        for (int s = 1; s < parts; ++s) {
-            const float4 v = *reinterpret_cast<const float4 *>(src + s * stride);
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+        float4 v[8];
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            if (s < parts) v[s] = *reinterpret_cast<const float4 *>(src + s * stride);
+        float4 acc = v[0];
+#pragma unroll
+        for (int s = 1; s < 8; ++s) {
+            if (s < parts) {
+                acc.x += v[s].x;
+                acc.y += v[s].y;
+                acc.z += v[s].z;
+                acc.w += v[s].w;
+            }
+        }
+        for (int s = 8; s < parts; ++s) {
+            const float4 w = *reinterpret_cast<const float4 *>(src + s * stride);
+            acc.x += w.x;
+            acc.y += w.y;
+            acc.z += w.z;
+            acc.w += w.w;
         }
         float *c = p.C + m * p.ldc + n;
         if (p.c_vec4 && n + 3 < p.N) {
@@ -1308,11 +1327,10 @@ cudaError_t launch_simt_tail_reduce(int config, int layout_b, int M, int N, int 
     const SimtParams p = simt_params(config, layout_b, M, N, K, C, ldc, c_vec4, lc, sk);
     if (p.tail_tiles == 0) return cudaSuccess;
     const SimtTile t = simt_tile(config, layout_b);
-    // about four blocks of 256 threads per SM in all, at most one per 256
-    // groups of 4 columns of a tile
+    // one group of 4 columns of a tile per thread (blocks of 256 threads)
     const int quads = t.bm * t.bn / 4;
-    const long long want = (4LL * (sm_count > 0 ? sm_count : 1) + p.tail_tiles - 1) / p.tail_tiles;
-    const int chunks = static_cast<int>(want < 1 ? 1 : want > quads / 256 ? quads / 256 : want);
+    const int chunks = quads / 256 > 0 ? quads / 256 : 1;
+    (void)sm_count;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.tail_tiles), static_cast<unsigned>(chunks > 0 ? chunks : 1), 1);
     cfg.blockDim = dim3(256, 1, 1);
