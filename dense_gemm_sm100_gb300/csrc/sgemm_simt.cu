@@ -1055,7 +1055,7 @@ void launch_cfg(int layout_b, const CUtensorMap &tmA, const CUtensorMap &tmB, co
 // warps of 8x8 with A loaded in pairs (256x128, 112 registers, spills: 59.3)
 // never win; they stay selectable.  With scalar FMAs instead of packed pairs
 // the 192x128 tile is issue-bound (57.7).
-ConfigEntry g_configs[] = {
+ConfigEntry g_tile_table[] = {
     DG_SIMT_CFG(4, 2, 8, 6, 8, 1, 0, true, 69.0f, 63.5f, "128x128"),
     DG_SIMT_CFG(4, 2, 8, 6, 8, 0, 0, false, 0.0f, 0.0f, "128x128s"),
     DG_SIMT_CFG(2, 2, 8, 4, 8, 1, 0, true, 58.9f, 51.4f, "64x128"),
@@ -1065,7 +1065,7 @@ ConfigEntry g_configs[] = {
     DG_SIMT_CFG(4, 4, 4, 6, 8, 1, 1, false, 66.6f, 0.0f, "128x128w16"),
     DG_SIMT_CFG(8, 2, 8, 4, 8, 1, 1, false, 0.0f, 0.0f, "256x128r"),
 };
-constexpr int kNumConfigs = sizeof(g_configs) / sizeof(g_configs[0]);
+constexpr int kNumConfigs = sizeof(g_tile_table) / sizeof(g_tile_table[0]);
 
 }  // namespace
 
@@ -1075,13 +1075,13 @@ cudaError_t prepare_simt()
     // refused by GEMM_OPT_SIMT_CONFIG); only the default one must work.
     for (int i = 0; i < kNumConfigs; ++i) {
         int ctas = 0;
-        cudaError_t e = g_configs[i].prepare(&ctas);
+        cudaError_t e = g_tile_table[i].prepare(&ctas);
         if (e != cudaSuccess) {
             (void)cudaGetLastError();
             if (i == 0) return e;
             ctas = 0;
         }
-        g_configs[i].ctas_per_sm = ctas;
+        g_tile_table[i].ctas_per_sm = ctas;
     }
     return cudaSuccess;
 }
@@ -1090,17 +1090,17 @@ int simt_num_configs() { return kNumConfigs; }
 
 bool simt_has_stream_k(int config)
 {
-    return config >= 0 && config < kNumConfigs && g_configs[config].stream_k;
+    return config >= 0 && config < kNumConfigs && g_tile_table[config].stream_k;
 }
 
 bool simt_config_usable(int config)
 {
-    return config >= 0 && config < kNumConfigs && g_configs[config].ctas_per_sm > 0;
+    return config >= 0 && config < kNumConfigs && g_tile_table[config].ctas_per_sm > 0;
 }
 
 SimtTile simt_tile(int config, int layout_b)
 {
-    const ConfigEntry &c = g_configs[config];
+    const ConfigEntry &c = g_tile_table[config];
     return SimtTile{c.bm, layout_b == 0 ? c.bn_row : c.bn_col, c.ctas_per_sm > 0 ? c.ctas_per_sm : 1, c.name};
 }
 
@@ -1150,7 +1150,7 @@ int simt_pick_config(int64_t M, int64_t N, int64_t K, int layout_b, int sm_count
     int best = 0;
     double best_cost = -1.0;
     for (int c = 0; c < kNumConfigs; ++c) {
-        const ConfigEntry &e = g_configs[c];
+        const ConfigEntry &e = g_tile_table[c];
         const float rate = layout_b == 0 ? e.rate_row : e.rate_col;
         if (rate <= 0.0f || e.ctas_per_sm <= 0) continue;
         const int64_t slots = max_ctas > 0 ? max_ctas : int64_t{sm_count} * e.ctas_per_sm;
@@ -1301,7 +1301,7 @@ cudaError_t launch_simt_f32(int config, const CUtensorMap &tmA, const CUtensorMa
                             const LaunchCommon &lc, const SplitK &sk)
 {
     const SimtParams p = simt_params(config, layout_b, M, N, K, C, ldc, c_vec4, lc, sk);
-    g_configs[config].launch(layout_b, tmA, tmB, p, lc.grid, lc.stream);
+    g_tile_table[config].launch(layout_b, tmA, tmB, p, lc.grid, lc.stream);
     return cudaGetLastError();
 }
 
@@ -1317,7 +1317,7 @@ cudaError_t launch_simt_f32_elementwise(int config, const float *A, int64_t lda,
     p.ew.ldb = ldb;
     CUtensorMap unused;
     memset(&unused, 0, sizeof unused);
-    g_configs[config].launch(3, unused, unused, p, lc.grid, lc.stream);
+    g_tile_table[config].launch(3, unused, unused, p, lc.grid, lc.stream);
     return cudaGetLastError();
 }
 
