@@ -179,9 +179,13 @@ int gemm_run(gemm_handle_t h, int layout_b, int64_t M, int64_t N, int64_t K,
  * previous block's C out run on two internal streams of the handle while a
  * block computes; events order the copies after the work already queued on
  * `stream` and make `stream` wait for the last copy, so the call behaves as
- * one operation on `stream`.  The result is bit-identical to gemm_run on the
- * same operands (no block is cut along K).  Pinned (page-locked) host memory
- * makes the copies asynchronous; pageable memory works but the copies block.
+ * one operation on `stream`.  Each block is a GEMM over the whole of K, but
+ * a block's partial last wave may be cut along K (slices or stream-K) where
+ * one call over the whole of C would cut other tiles, or none: the result
+ * then differs from gemm_run's by rounding only (the mode's tolerance), and
+ * is bit-identical where neither cuts a tile along K and on integer data.
+ * Pinned (page-locked) host memory makes the copies asynchronous; pageable
+ * memory works but the copies block.
  */
 int gemm_run_host(gemm_handle_t h, int layout_b, int64_t M, int64_t N, int64_t K,
                   const void *A_host, int64_t lda, const void *B_host, int64_t ldb,
