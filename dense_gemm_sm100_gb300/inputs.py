@@ -73,6 +73,10 @@ PROFILE_WORKLOADS = {
     # 19 x 32 tiles of 192 x 128 = 4 whole waves on 152 SMs; A, B, C 184 MiB
     "fp32_3648x4096x4096_row": Workload("fp32_3648x4096x4096_row", 3648, 4096, 4096, B_ROW_MAJOR,
                                         "uniform", 3),
+    # 20 x 32 tiles of 192 x 128 = 4 waves + 32 tiles: the last 32 shared out
+    # as stream-K ranges, as at 8192^3; A, B, C 190 MiB
+    "fp32_3840x4096x4096_row": Workload("fp32_3840x4096x4096_row", 3840, 4096, 4096, B_ROW_MAJOR,
+                                        "uniform", 3),
     # the same with B column-major (the corner-turning kernel)
     "fp32_3648x4096x4096_colB": Workload("fp32_3648x4096x4096_colB", 3648, 4096, 4096, B_COL_MAJOR,
                                          "uniform", 3),
