@@ -768,6 +768,23 @@ def main(argv=None):
             f = clocks["sm_mhz"] / peaks["sm_max_mhz"]
             r = main_res["roofline"]
             r["frac_at_observed_clock"] = round(r["achieved"] / (r["peak"] * f), 4) if f > 0 else None
+    e2e = None
+    if not args.no_e2e:
+        # Right after the headline leg, in the same thermal and power state
+        # (after the tensor-core modes' power-capped minutes the SM clock can
+        # sit lower); the host-buffer step moves 768 MiB over the host link:
+        # 10 steps.
+        esampler = ClockSampler(dev_index) if rank0 else None
+        if esampler:
+            esampler.start()
+        t_e0 = time.time()
+        r = bench_workload(g, args.workload, min(args.steps, 10), args.warmup, ctx, peaks,
+                           peak_note, with_e2e=True)
+        t_e1 = time.time()
+        e2e = r["e2e"]
+        if esampler:
+            esampler.stop()
+            e2e["clocks"] = esampler.summary(t_e0, t_e1)
     measured = None
     if not args.no_peaks:
         measured = measure_peaks(dev_index, peaks["sm_max_mhz"])
@@ -807,12 +824,6 @@ def main(argv=None):
                     m["roofline"]["frac_at_observed_clock"] = round(
                         m["roofline"]["achieved"] / (m["roofline"]["peak"] * f), 4) if f > 0 else None
             modes.append(m)
-    e2e = None
-    if not args.no_e2e:
-        # the host-buffer step moves 768 MiB over the host link: 10 steps
-        r = bench_workload(g, args.workload, min(args.steps, 10), args.warmup, ctx, peaks,
-                           peak_note, with_e2e=True)
-        e2e = r["e2e"]
     cpu = None
     if rank0 and ctx is None and not args.no_cpu_baseline:
         A64, B64, w, rows, threads = oracle_sample(args.workload, target_s=args.cpu_seconds)
