@@ -99,7 +99,7 @@ __device__ __forceinline__ void tile_coords(int t, const SimtParams &p, int &mb,
 }
 
 // Stream-K: the CTA owning iteration x of the tail, the last c with
-// floor(c * I / P) <= x (P = sk_parts <= I, so every range is non-empty
+// floor(c * I / P) <= x (P = sk.parts <= I, so every range is non-empty
 // and consecutive tiles' owners are consecutive CTAs).
 __device__ __forceinline__ long long sk_owner(long long x, const SimtParams &p)
 {
