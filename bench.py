@@ -42,6 +42,11 @@ TC_WORKLOADS = ["ffn_bf16_8192x14336x4096", "ffn_tf32_8192x14336x4096", "fp32x3_
 SIDE_ROUNDS = 5
 # The other specified FP32 workloads, measured under "modes" too.
 SIMT_WORKLOADS = ["fp32_128_row", "fp32_1024_colB", "fp32_4095x3073x2047_row"]
+# Launch-bound workloads: also timed as calls captured in a CUDA graph and
+# replayed (this library and the cuBLAS side reference alike), which takes
+# the per-call host and launch cost out of the time.
+GRAPH_WORKLOADS = ["fp32_128_row", "fp32_1024_colB"]
+GRAPH_CALLS, GRAPH_REPLAYS = 20, 10
 # Modes whose step is short run at least this many timed steps (recorded in
 # the mode's "steps"): the tensor-core modes reach their steady power state,
 # and the microsecond-scale FP32 cases get a stable mean.
@@ -214,6 +219,37 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- GPU timing
 
+def graph_us_per_call(fn, calls=GRAPH_CALLS, replays=GRAPH_REPLAYS):
+    """Capture `calls` calls of fn (which queues its work on the current
+    stream) in a CUDA graph, replay it, and return the device time per call
+    in microseconds (CUDA events around the replays)."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            fn()
+        side.synchronize()
+        with torch.cuda.graph(graph, stream=side):
+            for _ in range(calls):
+                fn()
+    torch.cuda.synchronize()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(replays):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (replays * calls)
+    del graph
+    torch.cuda.synchronize()
+    return us
+
+
 def time_device(run, stream, steps, warmup, counter=None):
     """Run `warmup` untimed steps, then `steps` timed steps with a CUDA event
     pair around each launch on `stream`.  Returns (total ms, per-step ms,
@@ -323,6 +359,20 @@ def bench_workload(g, name, steps, warmup, dist_ctx, peaks, peak_note, with_e2e,
     }
     if cub is not None:
         res["cublas_side"] = cub
+    if name in GRAPH_WORKLOADS:
+        def run_current():
+            g.run(A_d, B_d, C_d, w.layout_b, w.dtype, torch.cuda.current_stream())
+        us = graph_us_per_call(run_current)
+        res["graph"] = {"us_per_call": us, "tflops": w.flops / (us * 1e-6) / 1e12,
+                        "calls_per_graph": GRAPH_CALLS, "replays": GRAPH_REPLAYS}
+        if side_cublas:
+            Bl = B_d if w.layout_b == 0 else B_d.t()
+            cub_fn, _ = cublas_side_call(A_d, Bl, w.dtype)
+            torch.backends.cuda.matmul.allow_tf32 = w.dtype == "tf32"
+            cus = graph_us_per_call(cub_fn)
+            torch.backends.cuda.matmul.allow_tf32 = False
+            res["graph"]["cublas_us_per_call"] = cus
+            res["graph"]["cublas_tflops"] = w.flops / (cus * 1e-6) / 1e12
     if with_e2e:
         Ah = A.pin_memory()
         Bh = B.pin_memory()
@@ -815,6 +865,8 @@ def main(argv=None):
                 add_microbench(m["roofline"], mb)
             if "cublas_side" in r:
                 m["cublas_side"] = r["cublas_side"]
+            if "graph" in r:
+                m["graph"] = r["graph"]
             if msampler:
                 msampler.stop()
                 m["clocks"] = msampler.summary(*r["wall_window"])

@@ -811,3 +811,49 @@ def test_workspace_grows_in_stream_order(oracle_mod):
     for (A, B), (_, _, C) in zip(ops, outs):
         Cr, _ = oracle_of(oracle_mod, A, B, ROW)
         assert np.array_equal(to_f64(C), Cr)
+
+
+@pytest.mark.parametrize("mode,layout,shape", [
+    ("f32", ROW, (128, 128, 128)),     # one kernel
+    ("f32", COL, (1024, 1024, 1024)),  # re-pack-free stream-K: GEMM + dependent reduction kernel
+    ("f32", ROW, (301, 257, 131)),     # unaligned pitches: re-pack kernels first
+    ("bf16", ROW, (256, 512, 192)),    # tensor cores, pair MMA
+])
+def test_run_captures_in_a_cuda_graph(mode, layout, shape):
+    """gemm_run only queues work on the caller's stream (no host waits), so
+    a sequence of calls can be captured in a CUDA graph and replayed: the
+    replay gives the same bits as the calls run directly.  A first direct
+    call sizes the workspace, so nothing is allocated during the capture.
+    A handle of its own: the graph refers to its workspace."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dense_gemm_sm100_gb300 import gemm
+    M, N, K = shape
+    A, B = inp.make_operands(M, N, K, layout_b=layout, dist="normal", seed=M + 3 * N, dtype=mode)
+    dev = torch.device("cuda", 0)
+    A_d, B_d = A.to(dev), B.to(dev)
+    h = gemm.Gemm(0)
+    try:
+        C_direct = torch.empty((M, N), dtype=torch.float32, device=dev)
+        h.run(A_d, B_d, C_direct, layout, mode)
+        h.sync_status()
+        torch.cuda.synchronize()
+        C_graph = torch.full((M, N), float("nan"), dtype=torch.float32, device=dev)
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                for _ in range(3):
+                    h.run(A_d, B_d, C_graph, layout, mode, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        assert torch.isnan(C_graph).all()  # captured, not run
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
+        h.sync_status()
+        assert torch.equal(C_graph, C_direct)
+        del graph
+        torch.cuda.synchronize()
+    finally:
+        h.close()
