@@ -38,6 +38,7 @@ struct gemm_ctx {
     size_t ws_limit = 0;  // 0: none; else the workspace never grows beyond this many bytes
     int split_k = 0;      // 0: chosen per shape; 1: never; n > 1: n K slices (FP32 path)
     int stream_k = 0;     // FP32 tail: 0 chosen per shape, 1 slices, 2 stream-K
+    int simt_small = 0;   // FP32 small-problem kernel: 0 chosen per shape, 1 never, 2 always
     int tc_cluster = 3;   // tensor-core mode: 1 one CTA per tile, 3 pair MMA
     int tc_tma_store = 1; // tensor-core epilogue writes C with TMA stores when C allows it
     int tc_slices = 0;    // pair MMA: K slices per ring stage (0: library's choice)
@@ -123,6 +124,7 @@ bool tma_ready(const void *p, int64_t ld, int es)
 // Workspace a run needs: re-packed operands (when not TMA-ready) followed by
 // the split-K partial products of the FP32 path.
 struct PackPlan {
+    bool small = false;        // FP32 small-problem kernel: reads A and B where they are
     bool a = false, b = false;
     bool elementwise = false;  // FP32, row-major B: copy unaligned operands element-wise instead
     int64_t lda = 0, ldb = 0;
@@ -160,6 +162,12 @@ PackPlan plan_pack(const gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_
         pp.tc_split = dg::tc_pick_splits(dg::tc_units(M, N, cluster), slots, K3, 4, h->split_k);
         pp.split_bytes = static_cast<size_t>(
             round_up(static_cast<int64_t>(dg::tc_partial_bytes(M, N, pp.tc_split)), 256));
+        return pp;
+    }
+    if (dtype == GEMM_F32 && !h->force_repack &&
+        (h->simt_small == 2 || (h->simt_small == 0 && h->simt_config == 0 && h->max_ctas == 0 &&
+                                h->split_k == 0 && dg::simt_small_fits(M, N, K, h->sm_count)))) {
+        pp.small = true;  // no workspace: any pitch and alignment
         return pp;
     }
     const int es = elem_bytes(dtype);
@@ -387,7 +395,13 @@ int run_device(gemm_ctx *h, int layout_b, int64_t M, int64_t N, int64_t K, const
     lc.debug_drop = h->debug_drop;
     const char *lay = layout_b == GEMM_B_ROW_MAJOR ? "rowB" : "colB";
     int rc;
-    if (dtype == GEMM_F32) {
+    if (dtype == GEMM_F32 && pp.small) {
+        cudaError_t e = dg::launch_simt_small(layout_b, static_cast<const float *>(A), lda,
+                                              static_cast<const float *>(B), ldb, C, ldc, static_cast<int>(M),
+                                              static_cast<int>(N), static_cast<int>(K), stream);
+        if (e != cudaSuccess) return cuda_fail(h, e, "FP32 small-problem kernel launch");
+        path = std::string("simt_f32_small32x32_") + lay + path;
+    } else if (dtype == GEMM_F32) {
         const int cfg = pp.simt_config;
         const dg::SimtTile t = dg::simt_tile(cfg, layout_b);
         if (!pp.elementwise) {
@@ -920,6 +934,10 @@ int gemm_set_option(gemm_handle_t h, int option, int64_t value)
     case GEMM_OPT_STREAM_K:
         if (value < 0 || value > 2) break;
         h->stream_k = static_cast<int>(value);
+        return GEMM_OK;
+    case GEMM_OPT_SIMT_SMALL:
+        if (value < 0 || value > 2) break;
+        h->simt_small = static_cast<int>(value);
         return GEMM_OK;
     default:
         return fail(h, GEMM_ERR_INVALID, "unknown option");

@@ -49,6 +49,7 @@ GEMM_OPT_ELEMENTWISE = 11
 GEMM_OPT_WORKSPACE_LIMIT = 12
 GEMM_OPT_TC_STAGE_SLICES = 13
 GEMM_OPT_STREAM_K = 14
+GEMM_OPT_SIMT_SMALL = 15
 
 DTYPES = {"f32": GEMM_F32, "tf32": GEMM_TF32, "bf16": GEMM_BF16, "f32x3": GEMM_F32_3XTF32}
 LAYOUTS = {"row": GEMM_B_ROW_MAJOR, "col": GEMM_B_COL_MAJOR}

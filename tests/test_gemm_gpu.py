@@ -135,7 +135,8 @@ def test_unaligned_leading_dimensions(g, oracle_mod, mode, layout):
     address: re-packed first; FP32 with row-major B can instead copy them
     element by element into the shared-memory ring (cp.async,
     GEMM_OPT_ELEMENTWISE = 1).  Same bits either way, given the same K split
-    (the element-wise form has no stream-K, so both runs take slices)."""
+    (the element-wise form has no stream-K, so both runs take slices).  The
+    small-problem kernel, which reads any pitch where it is, is kept out."""
     from dense_gemm_sm100_gb300 import gemm
     M, N, K = 97, 203, 151
     A, B = inp.make_operands(M, N, K, layout_b=layout, seed=23, dist="normal", dtype=mode)
@@ -148,6 +149,7 @@ def test_unaligned_leading_dimensions(g, oracle_mod, mode, layout):
     Cbig = torch.zeros((M, N + 1), dtype=torch.float32, device=dev)
     C = Cbig[:, :N]
     g.set_option(gemm.GEMM_OPT_STREAM_K, 1)
+    g.set_option(gemm.GEMM_OPT_SIMT_SMALL, 1)
     try:
         g.run(Ap[:, 1:K + 1], Bp[:, 1:cols_b + 1], C, layout, mode)
         g.sync_status()
@@ -164,21 +166,26 @@ def test_unaligned_leading_dimensions(g, oracle_mod, mode, layout):
             assert torch.equal(C_first, C)
     finally:
         g.set_option(gemm.GEMM_OPT_STREAM_K, 0)
+        g.set_option(gemm.GEMM_OPT_SIMT_SMALL, 0)
     Cr, S = oracle_of(oracle_mod, A, B, layout)
     assert_parity(C, Cr, S, TOL[mode])
 
 
 @pytest.mark.parametrize("mode", MODES)
 def test_forced_repack_gives_same_bits(g, mode):
+    """The same persistent kernel on the operands in place and re-packed (the
+    small-problem kernel, which would take this shape, is kept out)."""
     from dense_gemm_sm100_gb300 import gemm
     A, B = inp.make_operands(160, 288, 192, seed=31, dtype=mode)
-    C1 = run_gpu(g, A, B, ROW, mode).cpu()
-    g.set_option(gemm.GEMM_OPT_FORCE_REPACK, 1)
+    g.set_option(gemm.GEMM_OPT_SIMT_SMALL, 1)
     try:
+        C1 = run_gpu(g, A, B, ROW, mode).cpu()
+        g.set_option(gemm.GEMM_OPT_FORCE_REPACK, 1)
         C2 = run_gpu(g, A, B, ROW, mode).cpu()
         assert "repack" in g.last_path
     finally:
         g.set_option(gemm.GEMM_OPT_FORCE_REPACK, 0)
+        g.set_option(gemm.GEMM_OPT_SIMT_SMALL, 0)
     assert torch.equal(C1, C2)
 
 
@@ -378,6 +385,7 @@ def test_workspace_limit_reports_nomem_without_launching(g, oracle_mod):
     try:
         h = gemm.Gemm(0)  # a fresh handle has no workspace yet
         h.set_option(gemm.GEMM_OPT_WORKSPACE_LIMIT, 4096)
+        h.set_option(gemm.GEMM_OPT_SIMT_SMALL, 1)  # the small-problem kernel would read in place
         with pytest.raises(gemm.GemmError) as err:
             h.run(A_d, B_d, C, ROW, "f32")
         assert err.value.code == gemm.GEMM_ERR_NOMEM
@@ -783,6 +791,7 @@ def test_workspace_grows_in_stream_order(oracle_mod):
     dev = torch.device("cuda", 0)
     shapes = [(300, 260, 130), (1100, 900, 700), (300, 260, 130)]
     with gemm.Gemm(0) as h:
+        h.set_option(gemm.GEMM_OPT_SIMT_SMALL, 1)  # the persistent kernels, whose operands get re-packed
         s1 = torch.cuda.Stream()
         ops, outs = [], []
         for i, (M, N, K) in enumerate(shapes):
@@ -816,7 +825,7 @@ def test_workspace_grows_in_stream_order(oracle_mod):
 @pytest.mark.parametrize("mode,layout,shape", [
     ("f32", ROW, (128, 128, 128)),     # one kernel
     ("f32", COL, (1024, 1024, 1024)),  # re-pack-free stream-K: GEMM + dependent reduction kernel
-    ("f32", ROW, (301, 257, 131)),     # unaligned pitches: re-pack kernels first
+    ("f32", ROW, (1301, 1257, 131)),   # unaligned pitches: re-pack kernels first
     ("bf16", ROW, (256, 512, 192)),    # tensor cores, pair MMA
 ])
 def test_run_captures_in_a_cuda_graph(mode, layout, shape):
@@ -857,3 +866,66 @@ def test_run_captures_in_a_cuda_graph(mode, layout, shape):
         torch.cuda.synchronize()
     finally:
         h.close()
+
+
+SMALL_KERNEL_SHAPES = [(1, 1, 1), (3, 5, 7), (32, 32, 32), (33, 31, 65), (128, 128, 128), (100, 300, 1000),
+                       (257, 129, 2049), (640, 96, 33)]
+
+
+@pytest.mark.parametrize("layout", [ROW, COL])
+@pytest.mark.parametrize("shape", SMALL_KERNEL_SHAPES)
+@pytest.mark.parametrize("pitch_pad", [0, 1])
+def test_small_kernel_matches_oracle(g, oracle_mod, layout, shape, pitch_pad):
+    """The FP32 small-problem kernel (32 x 32 tiles, 2 x 2 outputs per thread,
+    operands read in place at any pitch), forced on: ragged edges in every
+    dimension, K past one step and past 1024, 16-byte and odd pitches.  Same
+    tolerance as the other FP32 kernels, exact on integer inputs, and the
+    same bits as the persistent kernel without a K split (both add the k
+    products of an element in order with fused multiply-adds)."""
+    from dense_gemm_sm100_gb300 import gemm
+    M, N, K = shape
+    dev = torch.device("cuda", 0)
+
+    def placed(t):
+        if not pitch_pad:
+            return t.to(dev)
+        buf = torch.zeros((t.shape[0], t.shape[1] + pitch_pad), dtype=t.dtype, device=dev)
+        buf[:, :t.shape[1]] = t.to(dev)
+        return buf[:, :t.shape[1]]
+
+    A, B = inp.make_operands(M, N, K, layout_b=layout, dist="normal", seed=M + N + K + pitch_pad)
+    Ai, Bi = inp.make_integer_operands(M, N, K, layout_b=layout, seed=K + pitch_pad)
+    outs = []
+    g.set_option(gemm.GEMM_OPT_SIMT_SMALL, 2)
+    try:
+        for (a, b) in ((A, B), (Ai, Bi)):
+            C = torch.full((M, N), float("nan"), device=dev)
+            g.run(placed(a), placed(b), C, layout, "f32")
+            g.sync_status()
+            assert "small32x32" in g.last_path, g.last_path
+            outs.append(C.cpu())
+        g.set_option(gemm.GEMM_OPT_SIMT_SMALL, 1)
+        g.set_option(gemm.GEMM_OPT_SPLIT_K, 1)
+        C_tile = torch.empty((M, N), device=dev)
+        g.run(A.to(dev), B.to(dev), C_tile, layout, "f32")
+        g.sync_status()
+        assert "small" not in g.last_path, g.last_path
+    finally:
+        g.set_option(gemm.GEMM_OPT_SIMT_SMALL, 0)
+        g.set_option(gemm.GEMM_OPT_SPLIT_K, 0)
+    Cr, S = oracle_of(oracle_mod, A, B, layout)
+    assert_parity(outs[0], Cr, S, TOL["f32"], f"small kernel {shape}")
+    Cri, _ = oracle_of(oracle_mod, Ai, Bi, layout)
+    assert np.array_equal(to_f64(outs[1]), Cri)
+    assert torch.equal(outs[0], C_tile.cpu())
+
+
+def test_small_kernel_is_the_choice_for_a_few_tiles(g):
+    """128^3 (C1) is 16 tiles of 32 x 32 with K = 128: the small-problem kernel;
+    1024^3 (C2) is 1024 such tiles: the persistent kernels."""
+    A, B = inp.make_operands(128, 128, 128, seed=0)
+    run_gpu(g, A, B, ROW, "f32")
+    assert "small32x32" in g.last_path, g.last_path
+    A, B = inp.make_operands(1024, 1024, 1024, layout_b=COL, seed=1)
+    run_gpu(g, A, B, COL, "f32")
+    assert "small" not in g.last_path, g.last_path
