@@ -929,3 +929,34 @@ def test_small_kernel_is_the_choice_for_a_few_tiles(g):
     A, B = inp.make_operands(1024, 1024, 1024, layout_b=COL, seed=1)
     run_gpu(g, A, B, COL, "f32")
     assert "small" not in g.last_path, g.last_path
+
+
+def test_small_kernel_selection_bounds(g, oracle_mod):
+    """The small-problem kernel is chosen for K <= 256 and at most one 32 x 32
+    tile per SM, and not past either bound; GEMM_OPT_SIMT_CONFIG, MAX_CTAS
+    and SPLIT_K keep it out, SIMT_SMALL 1 never and 2 always uses it.  Every
+    run is checked against the oracle (exact on integer inputs)."""
+    from dense_gemm_sm100_gb300 import gemm
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+
+    def path_of(M, N, K, opts=()):
+        A, B = inp.make_integer_operands(M, N, K, layout_b=ROW, seed=M + N + K)
+        for k, v in opts:
+            g.set_option(k, v)
+        try:
+            C = run_gpu(g, A, B, ROW, "f32")
+        finally:
+            for k, _ in opts:
+                g.set_option(k, 0)
+        Cr, _ = oracle_of(oracle_mod, A, B, ROW)
+        assert np.array_equal(to_f64(C.cpu()), Cr), (M, N, K, opts)
+        return g.last_path
+
+    assert "small32x32" in path_of(96, 64, 256)
+    assert "small" not in path_of(96, 64, 257)
+    assert "small32x32" in path_of(32, 32 * sms, 64)        # one tile per SM
+    assert "small" not in path_of(32, 32 * sms + 1, 64)     # one tile more
+    for opt, val in ((gemm.GEMM_OPT_SIMT_CONFIG, 4), (gemm.GEMM_OPT_MAX_CTAS, 8), (gemm.GEMM_OPT_SPLIT_K, 1),
+                     (gemm.GEMM_OPT_SIMT_SMALL, 1)):
+        assert "small" not in path_of(128, 128, 128, ((opt, val),)), opt
+    assert "small32x32" in path_of(512, 512, 512, ((gemm.GEMM_OPT_SIMT_SMALL, 2),))
