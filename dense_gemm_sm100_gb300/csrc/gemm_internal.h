@@ -96,7 +96,7 @@ cudaError_t prepare_tc();
 
 // FP32 GEMM for small problems (sgemm_small.cu): one 32 x 32 tile of C per
 // CTA, A and B read at any pitch and alignment.  simt_small_fits: the
-// library's choice of it (at most one tile per SM, K <= 256).
+// library's choice of it (at most one tile per SM, K <= 384).
 bool simt_small_fits(int64_t M, int64_t N, int64_t K, int sm_count);
 cudaError_t launch_simt_small(int layout_b, const float *A, int64_t lda, const float *B, int64_t ldb, float *C,
                               int64_t ldc, int M, int N, int K, cudaStream_t stream);

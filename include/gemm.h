@@ -141,9 +141,11 @@ extern "C" {
  * (GEMM_OPT_SIMT_CONFIG 2, 5, 7, 8) and the element-wise producer
  * (GEMM_OPT_ELEMENTWISE) always take slices. */
 #define GEMM_OPT_STREAM_K 14
-/* FP32 small-problem kernel (one 32 x 32 tile of C per CTA, 2 x 2 outputs per
- * thread, A and B read at any pitch and alignment, no workspace): 0
- * (default) = used for problems of at most one tile per SM and K <= 256
+/* FP32 small-problem kernel (one 32 x 32 tile of C per CTA of 1024 threads in
+ * four K groups, 2 x 2 outputs per thread, the groups' partial tiles added in
+ * order in shared memory; A and B read at any pitch and alignment, no
+ * workspace): 0
+ * (default) = used for problems of at most one tile per SM and K <= 384
  * when GEMM_OPT_SIMT_CONFIG, GEMM_OPT_MAX_CTAS and GEMM_OPT_SPLIT_K are 0;
  * 1 = never; 2 = for every FP32 problem (tests). */
 #define GEMM_OPT_SIMT_SMALL 15
