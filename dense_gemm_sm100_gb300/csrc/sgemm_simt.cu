@@ -9,8 +9,10 @@
 //    in registers and does 8*TN FMAs per k from 8 A and TN B values.
 //  * 台阶 3/4 (vector loads, bank conflicts): the Tensor Memory Accelerator
 //    writes each stage with a 128-byte XOR swizzle; every shared load is a
-//    16-byte vector and the thread-to-data mapping below makes each warp-wide
-//    load hit 32 distinct banks (or broadcast).
+//    16-byte vector, and the thread-to-data mapping below puts the lanes of
+//    each quarter-warp on distinct bank groups or one broadcast address, so
+//    a load takes the wavefronts its pattern needs and no more (ncu counts
+//    bank conflicts at a fraction of a percent of the shared wavefronts).
 //  * 台阶 5 (warp tiling): a warp is 4 x 8 lanes covering 32 rows x 8*TN
 //    columns; lanes that share a row group share A loads.
 //  * 台阶 6/7 (double buffering, asynchronous copies): a dedicated producer

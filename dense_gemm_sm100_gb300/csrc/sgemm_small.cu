@@ -10,7 +10,8 @@
 // thread, and the groups' partial tiles are added in group order at the end
 // ("GEMM 性能优化", 台阶 1: K may be cut into slices whose partial products
 // add up to the product).  A and B go through shared memory 128 K at a time
-// (台阶 2: shared-memory tiling), the next chunk's global loads in flight
+// (台阶 1: shared-memory tiling), each thread keeps its outputs in registers
+// (台阶 2: thread tiling), and the next chunk's global loads are in flight
 // while the current one is multiplied (台阶 6, double buffering in
 // registers).  Each operand is staged in its own orientation, A and
 // column-major B K-contiguous and row-major B N-contiguous, so staging is a
